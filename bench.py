@@ -1,0 +1,564 @@
+"""Benchmark of the GB300 low-bit product library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
+
+Headline workload (the decode GEMV the metric is quoted on): Q2_0_g64 GEMV, 4096 x 4096 weights,
+batch 1, q8_0 activations.  One step = one pass of the decode hot path over one token: q8_0
+quantization of x [1][4096] followed by the GEMV against R = 64 distinct weight matrices (302 MB
+of packed weights, more than the 129 MB L2, so every step streams its weights from HBM).  The
+step's 65 launches are captured once in a CUDA graph and replayed.
+
+value       packed-weight bytes streamed per second (whole job, all ranks), weights resident in HBM
+e2e         the same metric through the public API with the token's activation copied from pinned
+            host memory and the step's outputs copied back, inside the timed region
+roofline    the dominant kernel (the GEMV) against the measured HBM copy bandwidth
+cpu_baseline the CPU oracle, as it stands, on a bounded sample of the same workload
+rows        the other hot-path rows (batch 8, Q1_0 / Q2_0_g64 Qwen3-8B-shaped token, planar
+            BitNet-2B4T token with its bf16 head), each measured the same way, outside the timed
+            region of the headline number
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the path shards by
+rows with no exchange, so no data-path collective is used); the timed region is bracketed by a
+barrier and the max time over ranks is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode GEMV packed-weight GB/s (% HBM peak); prefill GEMM int8 TOPS (% peak)"
+WORKLOAD = "Q2_0_g64 GEMV 4096x4096, batch 1, q8_0 activations (N(0,1)), codes -1/0/+1 at 31/38/31 %"
+N_ROT = 64
+ROWS_K = 4096
+ROWS_N = 4096
+
+
+def q2_bytes(N, K):
+    return N * (K // 64) * 18
+
+
+def q1_bytes(N, K):
+    return N * (K // 128) * 18
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks only)
+# ---------------------------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if not self.proc:
+            out["reasons"] = ["nvidia-smi unavailable"]
+            return out
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if sm:
+            out.update(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), samples=len(sm))
+        out["reasons"] = sorted(reasons)
+        return out
+
+
+# ---------------------------------------------------------------------------------------------
+# profile summary: DRAM traffic of the dominant kernel, valid only for the source it measured
+# ---------------------------------------------------------------------------------------------
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("lb_gemv.cu", "lb_common.cuh"):
+        with open(os.path.join(ROOT, "bit_matvec_lb_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(path_name: str):
+    path = os.path.join(ROOT, "profiles", path_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.]+)\s+source_sha:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_sha():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample, all host cores, rows split across threads)
+# ---------------------------------------------------------------------------------------------
+def oracle_gbs(blocks_np: np.ndarray, q, dx, budget_s: float, qk: int = 64):
+    import oracle
+    fn = oracle.q2_0_g64_product if qk == 64 else oracle.q1_0_product
+    cores = len(os.sched_getaffinity(0))
+    N = blocks_np.shape[0]
+    chunks = [blocks_np[i:i + max(1, N // cores)] for i in range(0, N, max(1, N // cores))]
+    fn(blocks_np[:8], q, dx, want_isum=False)  # build / warm
+    done_rows = 0
+    t0 = time.perf_counter()
+    reps = 0
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        while True:
+            list(ex.map(lambda c: fn(c, q, dx, want_isum=False), chunks))
+            reps += 1
+            done_rows += N
+            if time.perf_counter() - t0 >= budget_s:
+                break
+    dt = time.perf_counter() - t0
+    K = q.shape[1]
+    nbytes = done_rows * (K // qk) * 18
+    return nbytes / dt / 1e9, cores, reps, dt
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU workload helpers
+# ---------------------------------------------------------------------------------------------
+class Graph:
+    """Capture a sequence of library calls once and replay it."""
+
+    def __init__(self, fn, stream):
+        import torch
+        self.g = torch.cuda.CUDAGraph()
+        self.stream = stream
+        with torch.cuda.stream(stream):
+            fn()  # warm (also sets kernel attributes outside capture)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(self.g, stream=stream):
+            fn()
+
+    def replay(self):
+        self.g.replay()
+
+
+def time_graph(graph: Graph, reps: int, warm: int = 3) -> float:
+    """Average ms per replay, CUDA events on the capture stream."""
+    import torch
+    for _ in range(warm):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(graph.stream):
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def make_q2_weights(N, K, seed, device="cuda"):
+    """Random Q2_0_g64 weights in the repacked layout (code plane + fp16 scale plane)."""
+    import synth
+    codes = synth.device_q2_codes_packed(N * K // 4, seed, device=device)
+    scales = synth.device_fp16_scales(N * K // 64, seed + 7919, device=device)
+    return codes, scales
+
+
+def make_q1_weights(N, K, seed, device="cuda"):
+    import synth
+    bits = synth.device_bytes(N * K // 8, seed, device=device)
+    scales = synth.device_fp16_scales(N * K // 128, seed + 7919, device=device)
+    return bits, scales
+
+
+def headline(lb, args, dist, out):
+    import torch
+    import synth
+    import oracle
+
+    N, K = ROWS_N, ROWS_K
+    stream = torch.cuda.Stream()
+    # weights: AoS source blocks generated on the device, split by the library's repack
+    W = []
+    for r in range(N_ROT):
+        aos_codes = synth.device_q2_codes_packed(N * K // 4, seed=1000 * (dist.rank + 1) + r)
+        aos_scales = synth.device_fp16_scales(N * K // 64, seed=2000 * (dist.rank + 1) + r)
+        aos = torch.empty((N * K // 64, 18), dtype=torch.uint8, device="cuda")
+        aos[:, 0:2] = aos_scales.view(torch.uint8).view(-1, 2)
+        aos[:, 2:] = aos_codes.view(-1, 16)
+        codes = torch.empty(N * K // 4, dtype=torch.uint8, device="cuda")
+        scales = torch.empty(N * K // 64, dtype=torch.int16, device="cuda")
+        lb.lb_repack_q2_0_g64(aos, N, K, codes, scales)
+        W.append((codes, scales, aos if r == 0 else None))
+    torch.cuda.synchronize()
+    x_np = synth.activations(1, K, seed=1)
+    x = torch.from_numpy(x_np).cuda()
+    q = torch.empty((1, K), dtype=torch.int8, device="cuda")
+    d = torch.empty((1, K // 32), dtype=torch.int16, device="cuda")
+    Y = torch.empty((N_ROT, 1, N), dtype=torch.float32, device="cuda")
+
+    def step():
+        lb.lb_quantize_q8_0(x, q, d, 1, K, stream=stream)
+        for r in range(N_ROT):
+            lb.lb_gemv_q2_0_g64(W[r][0], W[r][1], q, d, Y[r], None, N, K, 1, stream=stream)
+
+    def gemvs_only():
+        for r in range(N_ROT):
+            lb.lb_gemv_q2_0_g64(W[r][0], W[r][1], q, d, Y[r], None, N, K, 1, stream=stream)
+
+    g_step = Graph(step, stream)
+    g_gemv = Graph(gemvs_only, stream)
+
+    # sanity: sampled rows of copy 0 against the oracle (outside any timed region)
+    torch.cuda.synchronize()
+    blocks0 = W[0][2].cpu().numpy().reshape(N, K // 64, 18)
+    q_ref, d_ref = oracle.quantize_q8_0(x_np)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    rows = np.arange(0, N, 257)
+    ref = oracle.q2_0_g64_product(blocks0[rows], q_ref, d_ref, want_isum=False)
+    err = np.abs(Y[0].cpu().numpy()[:, rows].astype(np.float64) - ref.y_exact)
+    assert np.all(err <= ref.tolerance()), "GPU output outside the oracle bound"
+
+    # ---- timed region ----
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(args.steps):
+            g_step.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = dist.max(e0.elapsed_time(e1) / args.steps)
+    step_bytes = N_ROT * q2_bytes(N, K)
+    value = step_bytes * dist.world / (ms * 1e-3) / 1e9
+
+    # ---- roofline: the GEMV alone, average launch duration over the same graph ----
+    hbm, peak_kind = peaks()
+    ms_gemv = time_graph(g_gemv, reps=max(50, args.steps // 4)) / N_ROT
+    alg_bytes = q2_bytes(N, K) + (K + K // 16) + 4 * N      # weights + q8_0 activation + y
+    achieved = alg_bytes / (ms_gemv * 1e-3) / 1e9
+    traffic = profiled_traffic("gemv_q2_0_g64_4096x4096_b1.md")
+
+    # ---- e2e: pinned host activation in, outputs out, every step ----
+    x_host = torch.from_numpy(x_np).pin_memory()
+    y_host = torch.empty((N_ROT, 1, N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(20, args.steps // 4)
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            x.copy_(x_host, non_blocking=True)
+            g_step.replay()
+            y_host.copy_(Y, non_blocking=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record()
+        for _ in range(e2e_steps):
+            x.copy_(x_host, non_blocking=True)
+            g_step.replay()
+            y_host.copy_(Y, non_blocking=True)
+        f1.record()
+    torch.cuda.synchronize()
+    ms_e2e = dist.max(f0.elapsed_time(f1) / e2e_steps)
+
+    out.update({
+        "value": round(value, 2), "ms_per_step": round(ms, 5),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
+                     "peak_kind": peak_kind, "kernel": "gemv_q_kernel<Q2_0_g64, B=1>",
+                     "alg_bytes_per_launch": alg_bytes, "avg_launch_us": round(ms_gemv * 1e3, 3)},
+        "e2e": {"value": round(step_bytes * dist.world / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(x_host.numel() * 4),
+                "d2h_bytes_per_step": int(y_host.numel() * 4)},
+        "clocks": clocks,
+        "gpu_launches": int(args.steps * (N_ROT + 1)),
+        "pct_hbm": round(100 * value / dist.world / hbm, 2),
+    })
+
+    if dist.rank == 0:
+        q_ref2 = q_ref
+        gbs, cores, reps, dt = oracle_gbs(blocks0[:512], q_ref2, d_ref, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                               "kind": "oracle",
+                               "sample": f"rows 0..511 of one 4096x4096 Q2_0_g64 matrix, batch 1, "
+                                         f"rows split over {cores} threads, {reps} passes in "
+                                         f"{dt:.1f} s"}
+    del W, g_step, g_gemv
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------------------------
+# other rows of the hot path (outside the headline timed region)
+# ---------------------------------------------------------------------------------------------
+def rows_measure(lb, out):
+    import torch
+    import synth
+    hbm, _ = peaks()
+    stream = torch.cuda.Stream()
+    rows = {}
+
+    # (1) config 2 at batch 8
+    N, K, B = ROWS_N, ROWS_K, 8
+    W = [make_q2_weights(N, K, 50_000 + r) for r in range(N_ROT)]
+    x = torch.from_numpy(synth.activations(B, K, seed=1)).cuda()
+    q = torch.empty((B, K), dtype=torch.int8, device="cuda")
+    d = torch.empty((B, K // 32), dtype=torch.int16, device="cuda")
+    Y = torch.empty((N_ROT, B, N), dtype=torch.float32, device="cuda")
+
+    def step_b8():
+        lb.lb_quantize_q8_0(x, q, d, B, K, stream=stream)
+        for r in range(N_ROT):
+            lb.lb_gemv_q2_0_g64(W[r][0], W[r][1], q, d, Y[r], None, N, K, B, stream=stream)
+    ms = time_graph(Graph(step_b8, stream), reps=50)
+    gbs = N_ROT * q2_bytes(N, K) / (ms * 1e-3) / 1e9
+    rows["q2_0_g64_4096x4096_b8"] = {"GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
+                                     "us_per_gemv": round(ms * 1e3 / N_ROT, 3)}
+    del W, Y
+    torch.cuda.empty_cache()
+
+    # (2) Qwen3-8B-shaped decode token, Q1_0 and Q2_0_g64, batch 1 (252 GEMVs, 36 layers)
+    for fmt in ("q2_0_g64", "q1_0"):
+        make = make_q2_weights if fmt == "q2_0_g64" else make_q1_weights
+        gemv = lb.lb_gemv_q2_0_g64 if fmt == "q2_0_g64" else lb.lb_gemv_q1_0
+        nbytes = q2_bytes if fmt == "q2_0_g64" else q1_bytes
+        layers = []
+        total = 0
+        for layer in range(synth.QWEN3_8B_LAYERS):
+            proj = []
+            for p, (name, n, k) in enumerate(synth.QWEN3_8B_PROJ):
+                proj.append((make(n, k, synth.proj_seed(60_000, layer, p)), n, k))
+                total += nbytes(n, k)
+            layers.append(proj)
+        xs = {k: torch.from_numpy(synth.activations(1, k, seed=k)).cuda() for k in (4096, 12288)}
+        qs = {k: torch.empty((1, k), dtype=torch.int8, device="cuda") for k in (4096, 12288)}
+        ds = {k: torch.empty((1, k // 32), dtype=torch.int16, device="cuda") for k in (4096, 12288)}
+        ybuf = torch.empty(12288, dtype=torch.float32, device="cuda")
+
+        def token():
+            for proj in layers:
+                for i, ((w, s), n, k) in enumerate(proj):
+                    if i in (0, 3, 6):   # new activation: attention input, attention output, FFN
+                        lb.lb_quantize_q8_0(xs[k], qs[k], ds[k], 1, k, stream=stream)
+                    gemv(w, s, qs[k], ds[k], ybuf, None, n, k, 1, stream=stream)
+        ms = time_graph(Graph(token, stream), reps=20)
+        gbs = total / (ms * 1e-3) / 1e9
+        rows[f"qwen3_8b_token_{fmt}_b1"] = {"GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
+                                            "ms_per_token": round(ms, 4), "bytes": total,
+                                            "launches": 36 * 10}
+        del layers
+        torch.cuda.empty_cache()
+
+    # (3) BitNet-2B4T-shaped token: planar body (210 GEMVs) + bf16 head 128256x2560, B=1 and 8
+    body = []
+    body_bytes = 0
+    for layer in range(synth.BITNET_2B4T_LAYERS):
+        for p, (name, n, k) in enumerate(synth.BITNET_2B4T_PROJ):
+            planes = synth.device_trit_planes(n, k, synth.proj_seed(70_000, layer, p))
+            body.append((planes, n, k))
+            body_bytes += n * k // 64 * 16
+    HN, HK = synth.BITNET_HEAD
+    head = synth.device_bytes(HN * HK * 2, 80_000).view(torch.int16)
+    head = (head & 0x3FFF) | 0x3C00  # finite bf16 patterns
+    for B in (1, 8):
+        x = torch.from_numpy(synth.activations(B, 6912, seed=2)).cuda()
+        xq = {k: (torch.empty((B, k), dtype=torch.int8, device="cuda"),
+                  torch.empty((B,), dtype=torch.float32, device="cuda")) for k in (2560, 6912)}
+        xh = torch.from_numpy(synth.activations(B, HK, seed=3)).cuda()
+        yb = torch.empty((B, 6912), dtype=torch.float32, device="cuda")
+        yh = torch.empty((B, HN), dtype=torch.float32, device="cuda")
+        x2560 = x[:, :2560].contiguous()
+
+        def token_bitnet():
+            for i, (planes, n, k) in enumerate(body):
+                if i % 7 in (0, 3, 6):
+                    src = x2560 if k == 2560 else x
+                    lb.lb_quantize_i8_absmax(src, xq[k][0], xq[k][1], B, k, stream=stream)
+                lb.lb_gemv_trit_planes(planes, 0.02, xq[k][0], xq[k][1], yb, None, n, k, B,
+                                       stream=stream)
+            lb.lb_gemv_bf16(head, xh, yh, HN, HK, B, stream=stream)
+
+        def head_only():
+            lb.lb_gemv_bf16(head, xh, yh, HN, HK, B, stream=stream)
+
+        ms = time_graph(Graph(token_bitnet, stream), reps=20)
+        ms_head = time_graph(Graph(head_only, stream), reps=20)
+        tot = body_bytes + HN * HK * 2
+        rows[f"bitnet_2b4t_token_b{B}"] = {
+            "GB/s": round(tot / (ms * 1e-3) / 1e9, 1), "pct_hbm": round(100 * tot / (ms * 1e-3) / 1e9 / hbm, 1),
+            "ms_per_token": round(ms, 4), "bytes": tot,
+            "head_GB/s": round(HN * HK * 2 / (ms_head * 1e-3) / 1e9, 1),
+            "body_GB/s": round(body_bytes / ((ms - ms_head) * 1e-3) / 1e9, 1)}
+    out["rows"] = rows
+
+
+# ---------------------------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands
+# ---------------------------------------------------------------------------------------------
+def reference_arm(args, dist, base):
+    if dist.rank != 0:
+        return None
+    import oracle
+    import synth
+    N, K = 512, ROWS_K
+    blocks = synth.q2_0_blocks(N, K, seed=0)
+    q, dx = oracle.quantize_q8_0(synth.activations(1, K, seed=1))
+    cores = len(os.sched_getaffinity(0))
+    chunks = [blocks[i:i + max(1, N // cores)] for i in range(0, N, max(1, N // cores))]
+
+    def one():
+        with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+            list(ex.map(lambda c: oracle.q2_0_g64_product(c, q, dx, want_isum=False), chunks))
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = q2_bytes(N, K) / dt / 1e9
+    sample = f"rows 0..{N - 1} of a 4096x4096 Q2_0_g64 matrix per step, batch 1, {cores} threads"
+    base.update({"impl": "reference", "value": round(value, 4), "ms_per_step": round(dt * 1e3, 3),
+                 "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                                  "kind": "oracle", "sample": sample},
+                 "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                         "d2h_bytes_per_step": 0}})
+    return base
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    dist = Dist()
+    base = {"metric": METRIC, "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic (seeded; random weights of the stated shapes and distributions)",
+            "config": {"workload": WORKLOAD, "weights_per_step": f"{N_ROT} distinct 4096x4096 "
+                       f"matrices, {N_ROT * q2_bytes(ROWS_N, ROWS_K)} B (> 129 MB L2)",
+                       "l2": "inputs larger than L2 (weight rotation)",
+                       "parallelism": f"replicas x{dist.world}"}}
+    if args.impl == "reference":
+        line = reference_arm(args, dist, base)
+        if line:
+            print(json.dumps(line))
+        dist.close()
+        return
+
+    import torch
+    import bit_matvec_lb_gb300 as lb
+    if dist.world == 1:
+        torch.cuda.set_device(0)
+    lb.load()
+    out = dict(base)
+    headline(lb, args, dist, out)
+    if dist.rank == 0 and dist.world == 1 and not args.no_rows:
+        rows_measure(lb, out)
+    if dist.rank == 0:
+        print(json.dumps(out))
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

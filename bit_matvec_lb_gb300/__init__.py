@@ -1,0 +1,149 @@
+"""Python binding of the GB300 low-bit product library (liblb.so, C ABI in include/lb.h).
+
+The functions here carry the C names and only marshal arguments: torch tensors (or raw integer
+device addresses) become pointers, the stream defaults to torch's current CUDA stream, and a
+non-zero status raises :class:`LBError`.  Every step of the computation runs in the library's
+CUDA kernels; there is no CPU or PyTorch fallback.  If the library is missing it is built with
+nvcc on first use; if that fails, or the device is not sm_103, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "LBError", "load", "library_path", "status_string",
+    "lb_quantize_q8_0", "lb_quantize_i8_absmax", "lb_repack_q1_0", "lb_repack_q2_0_g64",
+    "lb_gemv_q1_0", "lb_gemv_q2_0_g64", "lb_gemv_trit_planes", "lb_gemv_bf16",
+]
+
+LB_STATUS = {0: "LB_OK", -1: "LB_ERR_NULL", -2: "LB_ERR_ALIGN", -3: "LB_ERR_SHAPE",
+             -4: "LB_ERR_BATCH", -5: "LB_ERR_ARCH", -6: "LB_ERR_LAUNCH", -7: "LB_ERR_DEVICE"}
+
+
+class LBError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {status} ({LB_STATUS.get(status, 'LB_ERR_UNKNOWN')})")
+
+
+_lib = None
+_lock = threading.Lock()
+P = ctypes.c_void_p
+I64 = ctypes.c_int64
+I32 = ctypes.c_int
+F32 = ctypes.c_float
+
+SIGNATURES = {
+    "lb_status_string": (ctypes.c_char_p, [I32]),
+    "lb_version": (I32, []),
+    "lb_quantize_q8_0": (I32, [P, P, P, I64, I64, P]),
+    "lb_quantize_i8_absmax": (I32, [P, P, P, I64, I64, P]),
+    "lb_repack_q1_0": (I32, [P, I64, I64, P, P, P]),
+    "lb_repack_q2_0_g64": (I32, [P, I64, I64, P, P, P]),
+    "lb_gemv_q1_0": (I32, [P, P, P, P, P, P, I64, I64, I32, P]),
+    "lb_gemv_q2_0_g64": (I32, [P, P, P, P, P, P, I64, I64, I32, P]),
+    "lb_gemv_trit_planes": (I32, [P, F32, P, P, P, P, I64, I64, I32, P]),
+    "lb_gemv_bf16": (I32, [P, P, P, I64, I64, I32, P]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load liblb.so (building it with nvcc if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if build_if_missing and not _build.up_to_date():
+                path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"GB300 library not built: {path} is missing")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().lb_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        if not t.is_cuda:
+            raise ValueError("lb_* entry points take device tensors")
+        if not t.is_contiguous():
+            raise ValueError("lb_* entry points take contiguous tensors")
+        return t.data_ptr()
+    raise TypeError(f"cannot pass {type(t)} as a device pointer")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise LBError(fn, status)
+
+
+def lb_quantize_q8_0(x, q, d, B: int, K: int, stream=None):
+    _check("lb_quantize_q8_0", load().lb_quantize_q8_0(_ptr(x), _ptr(q), _ptr(d), B, K,
+                                                       _stream(stream)))
+
+
+def lb_quantize_i8_absmax(x, q, x_scale, B: int, K: int, stream=None):
+    _check("lb_quantize_i8_absmax", load().lb_quantize_i8_absmax(
+        _ptr(x), _ptr(q), _ptr(x_scale), B, K, _stream(stream)))
+
+
+def lb_repack_q1_0(blocks18, N: int, K: int, bits, scales, stream=None):
+    _check("lb_repack_q1_0", load().lb_repack_q1_0(_ptr(blocks18), N, K, _ptr(bits),
+                                                   _ptr(scales), _stream(stream)))
+
+
+def lb_repack_q2_0_g64(blocks18, N: int, K: int, codes, scales, stream=None):
+    _check("lb_repack_q2_0_g64", load().lb_repack_q2_0_g64(_ptr(blocks18), N, K, _ptr(codes),
+                                                           _ptr(scales), _stream(stream)))
+
+
+def lb_gemv_q1_0(bits, scales, q, d, y, isum, N: int, K: int, B: int, stream=None):
+    _check("lb_gemv_q1_0", load().lb_gemv_q1_0(_ptr(bits), _ptr(scales), _ptr(q), _ptr(d),
+                                               _ptr(y), _ptr(isum), N, K, B, _stream(stream)))
+
+
+def lb_gemv_q2_0_g64(codes, scales, q, d, y, isum, N: int, K: int, B: int, stream=None):
+    _check("lb_gemv_q2_0_g64", load().lb_gemv_q2_0_g64(
+        _ptr(codes), _ptr(scales), _ptr(q), _ptr(d), _ptr(y), _ptr(isum), N, K, B,
+        _stream(stream)))
+
+
+def lb_gemv_trit_planes(planes, w_scale: float, q, x_scale, y, acc, N: int, K: int, B: int,
+                        stream=None):
+    _check("lb_gemv_trit_planes", load().lb_gemv_trit_planes(
+        _ptr(planes), float(w_scale), _ptr(q), _ptr(x_scale), _ptr(y), _ptr(acc), N, K, B,
+        _stream(stream)))
+
+
+def lb_gemv_bf16(w, x, y, N: int, K: int, B: int, stream=None):
+    _check("lb_gemv_bf16", load().lb_gemv_bf16(_ptr(w), _ptr(x), _ptr(y), N, K, B,
+                                               _stream(stream)))

@@ -1,0 +1,99 @@
+// lb_capi.cu -- status names, version, and the device check shared by every entry point.
+//
+// Calls refuse with a reason and never fall back to another path: a device that is not
+// compute capability 10.3 gets LB_ERR_ARCH (the pages' rule for kernel selection is the same:
+// pin a kernel and error if the machine cannot run it, never fall back silently --
+// tritium.technology "Architecture", section 4.2).
+#include "lb_common.cuh"
+
+#include <mutex>
+#include <unordered_map>
+
+namespace lb {
+
+static constexpr int kMaxDevices = 64;
+static DeviceInfo g_info[kMaxDevices];
+static std::mutex g_info_mutex;
+
+int current_device_info(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return LB_ERR_ARCH;
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_info_mutex);
+        if (g_info[dev].ok < 0) {
+            int major = 0, minor = 0, sms = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                    cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                    cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                    cudaSuccess) {
+                cudaGetLastError();
+                return LB_ERR_ARCH;
+            }
+            g_info[dev].sms = sms;
+            g_info[dev].ok = (major == 10 && minor == 3) ? 1 : 0;
+        }
+        *out = g_info[dev];
+    }
+    return out->ok == 1 ? LB_OK : LB_ERR_ARCH;
+}
+
+struct KernelPrep {
+    bool attr_set = false;
+    size_t smem = (size_t)-1;
+    int threads = 0;
+    int blocks_per_sm = 0;
+};
+static std::unordered_map<const void *, KernelPrep> g_prep;
+static std::mutex g_prep_mutex;
+
+int prepare_kernel(const void *kernel, int threads, size_t smem, int *blocks_per_sm) {
+    std::lock_guard<std::mutex> lock(g_prep_mutex);
+    KernelPrep &p = g_prep[kernel];
+    if (!p.attr_set) {
+        int dev = 0, optin = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return LB_ERR_LAUNCH;
+        }
+        p.attr_set = true;
+    }
+    if (p.smem != smem || p.threads != threads) {
+        int bps = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel, threads, smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return LB_ERR_LAUNCH;
+        }
+        p.smem = smem;
+        p.threads = threads;
+        p.blocks_per_sm = bps;
+    }
+    *blocks_per_sm = p.blocks_per_sm;
+    return p.blocks_per_sm >= 1 ? LB_OK : LB_ERR_SHAPE;
+}
+
+}  // namespace lb
+
+LB_EXPORT const char *lb_status_string(int status) {
+    switch (status) {
+        case LB_OK: return "LB_OK";
+        case LB_ERR_NULL: return "LB_ERR_NULL";
+        case LB_ERR_ALIGN: return "LB_ERR_ALIGN";
+        case LB_ERR_SHAPE: return "LB_ERR_SHAPE";
+        case LB_ERR_BATCH: return "LB_ERR_BATCH";
+        case LB_ERR_ARCH: return "LB_ERR_ARCH";
+        case LB_ERR_LAUNCH: return "LB_ERR_LAUNCH";
+        case LB_ERR_DEVICE: return "LB_ERR_DEVICE";
+    }
+    return "LB_ERR_UNKNOWN";
+}
+
+LB_EXPORT int lb_version(void) { return 100; }

@@ -1,0 +1,145 @@
+/*
+ * lb.h -- C ABI of the GB300 (sm_103a) low-bit product library.
+ *
+ * The library computes the products of packed low-bit weights and quantized activations that
+ * dominate per-token time in low-bit LLM inference:
+ *   - ggml Q1_0     : 128 sign bits + an fp16 scale per 18-byte block;
+ *   - ggml Q2_0_g64 : 64 two-bit codes (code c means weight c-1) + an fp16 scale per 18 bytes;
+ *   - planar ternary: one 16-byte {u64 pos, u64 neg} beat per 64 columns of a row;
+ *   - a bf16 dense head.
+ *
+ * Sources the operations follow:
+ *   [TR] "bankml: verified low-bit inference on commodity CPUs -- a technical report",
+ *        sections III.2 (Q1_0 and its arithmetic), III.3 (float order, per-token activation
+ *        scales, prefill tile), III.5 (Q2_0_g64), III.8 (offset code).
+ *   [BH] bankml BUILD_HISTORY.md, ledger item "P2 -- own the kernels" (q8_0 quantizer: 127/amax,
+ *        round half to even; Q2_0 codes (v >> 2r) & 3).
+ *   [TA] tritium.technology "Architecture": section 1 (select-accumulate), 2 (bit planes),
+ *        3 (bf16 dense head), 4.1 (int32 accumulators, x = -128), 5 (w_scale and x_scale applied
+ *        as two multiplies).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise, allocated and owned
+ *     by the caller; the library allocates nothing and keeps no per-call state.
+ *   - Every pointer must be 16-byte aligned (LB_ERR_ALIGN otherwise).
+ *   - Matrices are row-major. Weights W are [N][K]: N output rows, K input columns.
+ *     Activations are token-major [B][K] (or [M][K]); outputs are [B][N] (or [M][N]) fp32.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Every call
+ *     only enqueues work on it and returns; results are ready when the stream is.
+ *   - Every call returns LB_OK (0) or a negative LB_ERR_* code. Arguments are checked on the
+ *     host before anything is enqueued; a refused call enqueues nothing. There is no fallback
+ *     path: a device that is not sm_103 is refused with LB_ERR_ARCH.
+ *   - Inputs must be finite; NaN or Inf activations give unspecified (but in-bounds) results.
+ *   - Calls that write the same output buffer must not overlap on the GPU.
+ */
+#ifndef LB_H_
+#define LB_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LB_OK 0
+#define LB_ERR_NULL (-1)    /* a required pointer is NULL */
+#define LB_ERR_ALIGN (-2)   /* a pointer is not 16-byte aligned */
+#define LB_ERR_SHAPE (-3)   /* a size is out of range or not a multiple of the block */
+#define LB_ERR_BATCH (-4)   /* GEMV batch outside [1, 8] */
+#define LB_ERR_ARCH (-5)    /* the current device is not compute capability 10.3 */
+#define LB_ERR_LAUNCH (-6)  /* the CUDA launch failed (the CUDA error is left pending) */
+#define LB_ERR_DEVICE (-7)  /* a device-side check failed (reported through dev_err) */
+
+/* Name of a status code ("LB_OK", "LB_ERR_SHAPE", ...); never NULL. */
+const char *lb_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int lb_version(void);
+
+/* ---------------------------------------------------------------------------------------
+ * Activation quantizers
+ * ------------------------------------------------------------------------------------- */
+
+/* q8_0 ([TR] III.2, [BH]): for every token b and every block of 32 values,
+ *   amax = max|x|, d = fp16_rne(amax / 127), id = amax != 0 ? 127 / amax : 0,
+ *   q[i] = round_half_even(x[i] * id)  (binary32 arithmetic, IEEE division).
+ *   x : [B][K] fp32.   q : [B][K] int8 (codes in [-127, 127]).
+ *   d : [B][K/32] fp16 bit patterns.
+ * K % 32 == 0, K >= 32, B >= 1 (LB_ERR_SHAPE otherwise). */
+int lb_quantize_q8_0(const float *x, int8_t *q, uint16_t *d, int64_t B, int64_t K,
+                     void *stream);
+
+/* Per-token absmax int8 for the planar path (the pages say only "int8 activations"; the
+ * reading is the plainest one): amax = max_k |x[b][k]|, s = amax != 0 ? 127/amax : 0,
+ *   q[b][k] = clamp(round_half_even(x[b][k] * s), -128, 127), x_scale[b] = amax / 127.
+ *   x : [B][K] fp32.  q : [B][K] int8.  x_scale : [B] fp32.
+ * K % 16 == 0, K >= 16, B >= 1. */
+int lb_quantize_i8_absmax(const float *x, int8_t *q, float *x_scale, int64_t B, int64_t K,
+                          void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Load-time repack: split the 18-byte source blocks into two aligned planes.
+ *   blocks18 : [N][K/QK][18] source bytes (fp16 d little-endian, then 16 data bytes);
+ *              QK = 128 for Q1_0, 64 for Q2_0_g64. This pointer needs no alignment.
+ *   bits     : [N][K/QK * 16] data bytes, bit order unchanged.
+ *   scales   : [N][K/QK] fp16 bit patterns.
+ * Q1_0: K % 128 == 0. Q2_0_g64: K % 64 == 0. N >= 1.
+ * ------------------------------------------------------------------------------------- */
+int lb_repack_q1_0(const void *blocks18, int64_t N, int64_t K, uint8_t *bits, uint16_t *scales,
+                   void *stream);
+int lb_repack_q2_0_g64(const void *blocks18, int64_t N, int64_t K, uint8_t *codes,
+                       uint16_t *scales, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Decode GEMVs (batch B in [1, 8] tokens sharing the weights)
+ * ------------------------------------------------------------------------------------- */
+
+/* Q1_0 x q8_0 ([TR] III.2-III.3). For token b, row n, weight block k (128 weights) and its
+ * four q8_0 blocks j:
+ *   isum_j = sum_{i in j} s_i * q_i  (s_i = +1 for a set bit, -1 otherwise; integer, exact)
+ *   y[b][n] = sum_k d_w[n][k] * sum_j d_x[b][j] * isum_j      (fp32 accumulation)
+ *   bits   : [N][K/8] repacked sign bytes (lb_repack_q1_0).   scales : [N][K/128] fp16.
+ *   q, d   : q8_0 activations [B][K] int8, [B][K/32] fp16 (lb_quantize_q8_0 layout).
+ *   y      : [B][N] fp32.
+ *   isum_opt : NULL, or [B][N][K/32] int32 that receives every isum_j (a test hook; the same
+ *              kernel writes it).
+ * Accuracy: |y - exact| <= 1e-5 * sum |d_w d_x isum| + 1e-6, where exact is the real-number
+ * value of the formula above. K % 128 == 0; N >= 1; B in [1, 8]. */
+int lb_gemv_q1_0(const uint8_t *bits, const uint16_t *scales, const int8_t *q,
+                 const uint16_t *d, float *y, int32_t *isum_opt, int64_t N, int64_t K, int B,
+                 void *stream);
+
+/* Q2_0_g64 x q8_0 ([TR] III.5, III.8): as lb_gemv_q1_0 with 64-weight blocks, weight i of a
+ * block = ((codes byte i/4) >> 2*(i%4)) & 3, minus 1, in {-1, 0, +1, +2}, and two q8_0
+ * blocks per weight block.
+ *   codes : [N][K/4] repacked code bytes (lb_repack_q2_0_g64).   scales : [N][K/64] fp16.
+ * K % 64 == 0; N >= 1; B in [1, 8]. */
+int lb_gemv_q2_0_g64(const uint8_t *codes, const uint16_t *scales, const int8_t *q,
+                     const uint16_t *d, float *y, int32_t *isum_opt, int64_t N, int64_t K,
+                     int B, void *stream);
+
+/* Planar ternary select-accumulate ([TA] 1, 2, 4.1, 5):
+ *   acc[b][r] = sum_{c: pos bit set} q[b][c] - sum_{c: neg bit set} q[b][c]   (int32, exact,
+ *               correct for q = -128)
+ *   y[b][r]   = (float(acc) * x_scale[b]) * w_scale   (two binary32 roundings, in this order)
+ *   planes  : [N][K/64][2] u64, beat g of row r = {pos, neg}, bit c <-> column 64g + c,
+ *             little-endian. A column set in both planes gives an unspecified result.
+ *   q       : [B][K] int8.   x_scale : [B] fp32.   y : [B][N] fp32.
+ *   acc_opt : NULL, or [B][N] int32 that receives acc.
+ * K % 64 == 0; K <= 2^24 / 128 (so acc is exact in int32 and in binary32); N >= 1; B in [1,8].*/
+int lb_gemv_trit_planes(const uint64_t *planes, float w_scale, const int8_t *q,
+                        const float *x_scale, float *y, int32_t *acc_opt, int64_t N, int64_t K,
+                        int B, void *stream);
+
+/* Dense bf16 head ([TA] 3): y[b][n] = sum_k float(W[n][k]) * x[b][k], fp32 accumulation,
+ * bf16 widened exactly (16-bit left shift).
+ *   w : [N][K] bf16 bit patterns.   x : [B][K] fp32.   y : [B][N] fp32.
+ * Accuracy: |y - exact| <= 1e-5 * sum_k |w x| + 1e-6. K % 8 == 0; N >= 1; B in [1, 8]. */
+int lb_gemv_bf16(const uint16_t *w, const float *x, float *y, int64_t N, int64_t K, int B,
+                 void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LB_H_ */

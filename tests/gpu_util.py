@@ -1,0 +1,70 @@
+"""Helpers for the GPU parity tests: move numpy arrays to the device and call the C ABI."""
+import numpy as np
+import torch
+
+import bit_matvec_lb_gb300 as lb
+
+_VIEW = {np.dtype(np.uint16): np.int16, np.dtype(np.uint32): np.int32,
+         np.dtype(np.uint64): np.int64}
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if a.dtype in _VIEW:
+        a = a.view(_VIEW[a.dtype])
+    return torch.from_numpy(a).cuda()
+
+
+def host(t: torch.Tensor, dtype=None) -> np.ndarray:
+    a = t.detach().cpu().numpy()
+    return a.view(dtype) if dtype is not None else a
+
+
+def repack_on_gpu(blocks: np.ndarray, K: int, qk: int):
+    N = blocks.shape[0]
+    src = dev(blocks.reshape(-1))
+    bits = torch.empty(N * (K // qk) * 16, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(N * (K // qk), dtype=torch.int16, device="cuda")
+    fn = lb.lb_repack_q1_0 if qk == 128 else lb.lb_repack_q2_0_g64
+    fn(src, N, K, bits, scales)
+    return bits, scales
+
+
+def gemv_q(qk: int, blocks: np.ndarray, q: np.ndarray, dx: np.ndarray, want_isum=True):
+    """Run lb_gemv_q1_0 (qk=128) or lb_gemv_q2_0_g64 (qk=64); returns (y, isum or None)."""
+    N = blocks.shape[0]
+    B, K = q.shape
+    bits, scales = repack_on_gpu(blocks, K, qk)
+    y = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
+    isum = torch.empty((B, N, K // 32), dtype=torch.int32, device="cuda") if want_isum else None
+    fn = lb.lb_gemv_q1_0 if qk == 128 else lb.lb_gemv_q2_0_g64
+    fn(bits, scales, dev(q), dev(dx), y, isum, N, K, B)
+    torch.cuda.synchronize()
+    return host(y), (host(isum) if want_isum else None)
+
+
+def gemv_trit(planes: np.ndarray, w_scale: float, q: np.ndarray, x_scale: np.ndarray):
+    N = planes.shape[0]
+    B, K = q.shape
+    y = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
+    acc = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    lb.lb_gemv_trit_planes(dev(planes), w_scale, dev(q), dev(x_scale.astype(np.float32)), y, acc,
+                           N, K, B)
+    torch.cuda.synchronize()
+    return host(acc), host(y)
+
+
+def gemv_bf16(w: np.ndarray, x: np.ndarray):
+    N, K = w.shape
+    B = x.shape[0]
+    y = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
+    lb.lb_gemv_bf16(dev(w), dev(x), y, N, K, B)
+    torch.cuda.synchronize()
+    return host(y)
+
+
+def within(y, y_exact, mag, rel=1e-5, abs_=1e-6):
+    err = np.abs(y.astype(np.float64) - y_exact)
+    tol = rel * mag + abs_
+    ok = err <= tol
+    return bool(np.all(ok)), float(np.max(err / tol)) if err.size else 0.0

@@ -1,0 +1,118 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point include/lb.h declares,
+and refuses bad arguments on the host before touching the device (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_matvec_lb_gb300 as lb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def declared_symbols():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(lb_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return lb.load()
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for expected in ("lb_quantize_q8_0", "lb_repack_q1_0", "lb_repack_q2_0_g64",
+                     "lb_gemv_q1_0", "lb_gemv_q2_0_g64", "lb_gemv_trit_planes", "lb_gemv_bf16",
+                     "lb_status_string"):
+        assert expected in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, f"declared in include/*.h but not exported: {missing}"
+
+
+def test_binding_names_match_header():
+    for n in declared_symbols():
+        if n in ("lb_status_string", "lb_version"):
+            continue
+        assert hasattr(lb, n), f"python binding lacks {n}"
+        assert n in lb.SIGNATURES
+
+
+def test_status_strings(lib):
+    for code, name in lb.LB_STATUS.items():
+        assert lib.lb_status_string(code).decode() == name
+    assert lib.lb_status_string(12345).decode() == "LB_ERR_UNKNOWN"
+    assert lib.lb_version() >= 100
+
+
+# Host-side refusals: these return before any CUDA call, so they run without a GPU.
+A = 0x10000          # 16-byte aligned fake device address (never dereferenced)
+MIS = 0x10008        # misaligned
+
+
+def test_refuse_null(lib):
+    assert lib.lb_gemv_q1_0(None, A, A, A, A, None, 4, 128, 1, None) == -1
+    assert lib.lb_gemv_q2_0_g64(A, A, A, A, None, None, 4, 64, 1, None) == -1
+    assert lib.lb_gemv_trit_planes(A, 1.0, A, None, A, None, 4, 64, 1, None) == -1
+    assert lib.lb_gemv_bf16(A, None, A, 4, 8, 1, None) == -1
+    assert lib.lb_quantize_q8_0(A, None, A, 1, 32, None) == -1
+    assert lib.lb_repack_q1_0(None, 1, 128, A, A, None) == -1
+
+
+def test_refuse_misaligned(lib):
+    assert lib.lb_gemv_q1_0(MIS, A, A, A, A, None, 4, 128, 1, None) == -2
+    assert lib.lb_gemv_q2_0_g64(A, A, A, A, A, MIS, 4, 64, 1, None) == -2
+    assert lib.lb_gemv_trit_planes(A, 1.0, A, A, MIS, None, 4, 64, 1, None) == -2
+    assert lib.lb_gemv_bf16(A, A, MIS, 4, 8, 1, None) == -2
+    assert lib.lb_quantize_q8_0(MIS, A, A, 1, 32, None) == -2
+
+
+@pytest.mark.parametrize("K", [0, 64, 192, 100])
+def test_refuse_q1_shape(lib, K):
+    assert lib.lb_gemv_q1_0(A, A, A, A, A, None, 4, K, 1, None) == -3
+
+
+def test_refuse_other_shapes(lib):
+    assert lib.lb_gemv_q2_0_g64(A, A, A, A, A, None, 4, 96, 1, None) == -3
+    assert lib.lb_gemv_q2_0_g64(A, A, A, A, A, None, 0, 64, 1, None) == -3
+    assert lib.lb_gemv_trit_planes(A, 1.0, A, A, A, None, 4, 32, 1, None) == -3
+    assert lib.lb_gemv_trit_planes(A, 1.0, A, A, A, None, 4, 262144, 1, None) == -3
+    assert lib.lb_gemv_bf16(A, A, A, 4, 12, 1, None) == -3
+    assert lib.lb_quantize_q8_0(A, A, A, 1, 48, None) == -3
+    assert lib.lb_quantize_q8_0(A, A, A, 0, 32, None) == -3
+    assert lib.lb_repack_q2_0_g64(A, 2, 100, A, A, None) == -3
+
+
+@pytest.mark.parametrize("B", [0, 9, -1])
+def test_refuse_batch(lib, B):
+    assert lib.lb_gemv_q1_0(A, A, A, A, A, None, 4, 128, B, None) == -4
+    assert lib.lb_gemv_q2_0_g64(A, A, A, A, A, None, 4, 64, B, None) == -4
+    assert lib.lb_gemv_trit_planes(A, 1.0, A, A, A, None, 4, 64, B, None) == -4
+    assert lib.lb_gemv_bf16(A, A, A, 4, 8, B, None) == -4
+
+
+def test_refuse_without_sm103(lib):
+    """Valid arguments on a machine whose current device is not an sm_103 GPU (or that has
+    no GPU at all) are refused with LB_ERR_ARCH -- there is no fallback path."""
+    import torch
+    if torch.cuda.is_available():
+        major, minor = torch.cuda.get_device_capability()
+        if (major, minor) == (10, 3):
+            pytest.skip("an sm_103 device is present")
+    assert lib.lb_gemv_q1_0(A, A, A, A, A, None, 4, 128, 1, None) == -5
+
+
+def test_python_binding_raises_on_error():
+    with pytest.raises(lb.LBError) as e:
+        lb.lb_gemv_bf16(A, A, A, 4, 12, 1, stream=0)
+    assert e.value.status == -3 and "LB_ERR_SHAPE" in str(e.value)

@@ -1,0 +1,262 @@
+"""GPU parity: every CUDA entry point against the CPU oracle, on the same seeded inputs.
+
+Bars: integer results (q8_0 codes and scales, repacked planes, Q1_0/Q2_0_g64 block sums, planar
+accumulators and planar outputs) bit-exact; fp32 outputs of the Q1_0 / Q2_0_g64 / bf16 products
+within |y - exact| <= 1e-5 * sum|terms| + 1e-6.  Sizes span several tiles and ragged tails, batch
+1..8, the degenerate cases (code +2, all -128 activations, zero blocks, unit scales) and the
+full workload shapes (full comparison where the oracle is fast enough, sampled rows otherwise).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_matvec_lb_gb300 as lb
+import oracle
+import synth
+from gpu_util import dev, gemv_bf16, gemv_q, gemv_trit, host, repack_on_gpu, within
+
+pytestmark = pytest.mark.gpu
+
+
+def _q8(B, K, seed):
+    return oracle.quantize_q8_0(synth.activations(B, K, seed))
+
+
+# ----------------------------------------------------------------------------------------------
+# quantizers and repack
+# ----------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B,K", [(1, 32), (3, 96), (1, 512), (8, 4096), (2, 12288), (512, 4096)])
+def test_quantize_q8_0(B, K):
+    x = synth.activations(B, K, seed=B * 7 + K)
+    x[0, :32] = 0.0                                    # an all-zero block
+    if K >= 64:
+        x[0, 32:64] *= 1e4                              # a large block
+    q_ref, d_ref = oracle.quantize_q8_0(x)
+    q = torch.empty((B, K), dtype=torch.int8, device="cuda")
+    d = torch.empty((B, K // 32), dtype=torch.int16, device="cuda")
+    lb.lb_quantize_q8_0(dev(x), q, d, B, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(q), q_ref)
+    assert np.array_equal(host(d, np.uint16), d_ref)
+
+
+def test_quantize_q8_0_ties():
+    from golden_io import read
+    gd = read("q8_0_ties.txt")
+    x = np.array([[float(t) for t in gd["x"].split()]], dtype=np.float32)
+    q = torch.empty((1, 32), dtype=torch.int8, device="cuda")
+    d = torch.empty((1, 1), dtype=torch.int16, device="cuda")
+    lb.lb_quantize_q8_0(dev(x), q, d, 1, 32)
+    torch.cuda.synchronize()
+    assert host(q)[0].tolist() == [int(t) for t in gd["q"].split()]
+    assert int(host(d, np.uint16)[0, 0]) == int(gd["d"], 16)
+
+
+@pytest.mark.parametrize("B,K", [(1, 16), (1, 2560), (8, 2560), (3, 6912)])
+def test_quantize_i8_absmax(B, K):
+    x = synth.activations(B, K, seed=K + B)
+    if B > 1:
+        x[1] = 0.0
+    q_ref, s_ref = oracle.quantize_i8_absmax(x)
+    q = torch.empty((B, K), dtype=torch.int8, device="cuda")
+    s = torch.empty((B,), dtype=torch.float32, device="cuda")
+    lb.lb_quantize_i8_absmax(dev(x), q, s, B, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(q), q_ref)
+    assert np.array_equal(host(s).view(np.uint32), s_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("qk,N,K", [(128, 5, 384), (64, 7, 320), (128, 300, 4096), (64, 129, 4096)])
+def test_repack(qk, N, K):
+    blocks = synth.q1_0_blocks(N, K, seed=1) if qk == 128 else synth.q2_0_blocks(N, K, seed=2)
+    bits, scales = repack_on_gpu(blocks, K, qk)
+    torch.cuda.synchronize()
+    b_ref, s_ref = oracle.repack(blocks, K, qk)
+    assert np.array_equal(host(bits).reshape(N, -1), b_ref)
+    assert np.array_equal(host(scales, np.uint16).reshape(N, -1), s_ref)
+
+
+# ----------------------------------------------------------------------------------------------
+# Q1_0 / Q2_0_g64 GEMV
+# ----------------------------------------------------------------------------------------------
+def _check_q(qk, blocks, q, dx, want_isum=True):
+    ref = (oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product)(blocks, q, dx)
+    y, isum = gemv_q(qk, blocks, q, dx, want_isum=want_isum)
+    if want_isum:
+        assert np.array_equal(isum, ref.isum), "integer block sums differ"
+    ok, worst = within(y, ref.y_exact, ref.mag)
+    assert ok, f"fp32 output outside the bound (worst err/tol = {worst:.3g})"
+    return y, ref
+
+
+def test_q1_0_tiny_config():
+    """Q1_0 GEMV tiny: W 256x512, sign bits p=0.5, fp16 |N(0,0.02)| scales, x N(0,1) -> q8_0,
+    batch 1, seed 0."""
+    blocks = synth.q1_0_blocks(256, 512, seed=0)
+    q, dx = oracle.quantize_q8_0(synth.activations(1, 512, seed=0))
+    _check_q(128, blocks, q, dx)
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_q1_0_ragged(B):
+    N, K = 37, 384 if B % 2 else 4224          # 3 or 33 blocks per row: ragged lane coverage
+    blocks = synth.q1_0_blocks(N, K, seed=100 + B)
+    q, dx = _q8(B, K, seed=200 + B)
+    _check_q(128, blocks, q, dx)
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_q2_0_ragged(B):
+    N, K = 41, 320 if B % 2 else 4160          # 5 or 65 blocks per row
+    blocks = synth.q2_0_blocks(N, K, seed=300 + B, probs=(0.25, 0.25, 0.25, 0.25))
+    q, dx = _q8(B, K, seed=400 + B)
+    _check_q(64, blocks, q, dx)
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_q2_0_config_4096(B):
+    """Q2_0_g64 GEMV 4096x4096, codes {-1,0,+1} at 31/38/31 %, batch 1 and 8 (full compare)."""
+    blocks = synth.q2_0_blocks(4096, 4096, seed=0)
+    q, dx = _q8(B, 4096, seed=1)
+    _check_q(64, blocks, q, dx, want_isum=(B == 1))
+
+
+@pytest.mark.parametrize("qk", [128, 64])
+def test_production_path_matches_hooked_path(qk):
+    """The production instantiation (no block-sum hook) gives the same outputs."""
+    N, K, B = 300, 4096, 2
+    blocks = synth.q1_0_blocks(N, K, seed=5) if qk == 128 else synth.q2_0_blocks(N, K, seed=5)
+    q, dx = _q8(B, K, seed=6)
+    y1, _ = gemv_q(qk, blocks, q, dx, want_isum=True)
+    y0, _ = gemv_q(qk, blocks, q, dx, want_isum=False)
+    ref = (oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product)(blocks, q, dx)
+    assert within(y0, ref.y_exact, ref.mag)[0]
+    assert within(y1, ref.y_exact, ref.mag)[0]
+
+
+@pytest.mark.parametrize("qk", [128, 64])
+def test_minus128_extremes(qk):
+    """Hand-built activation blocks of -128/-127/127 codes (never produced by the quantizer,
+    accepted by the kernels): the integer sums must stay exact."""
+    N, K, B = 33, 1024, 3
+    blocks = (synth.q1_0_blocks(N, K, seed=9) if qk == 128
+              else synth.q2_0_blocks(N, K, seed=9, probs=(0.3, 0.1, 0.3, 0.3)))
+    q = synth.int8_codes(B, K, seed=10, extremes=True)
+    q[0] = -128
+    dx = synth.q8_scales(B, K, seed=11)
+    _check_q(qk, blocks, q, dx)
+
+
+@pytest.mark.parametrize("qk", [128, 64])
+def test_unit_scales_exact(qk):
+    """With every scale 1.0 each fp32 partial is an integer below 2^24: y == sum isum exactly."""
+    N, K, B = 70, 2048, 2
+    one = np.float16(1.0).view(np.uint16)
+    nb = K // qk
+    sc = np.full((N, nb), one, np.uint16)
+    blocks = (synth.q1_0_blocks(N, K, seed=12, scales=sc) if qk == 128
+              else synth.q2_0_blocks(N, K, seed=12, scales=sc, probs=(0.25,) * 4))
+    q = synth.int8_codes(B, K, seed=13)
+    dx = np.full((B, K // 32), one, np.uint16)
+    y, isum = gemv_q(qk, blocks, q, dx)
+    assert np.array_equal(y.astype(np.int64), isum.astype(np.int64).sum(-1))
+    ref = (oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product)(blocks, q, dx)
+    assert np.array_equal(isum, ref.isum)
+
+
+def test_zero_scales_and_zero_activations():
+    N, K, B = 16, 512, 2
+    blocks = synth.q2_0_blocks(N, K, seed=14)
+    blocks[:, :, :2] = 0                                   # d_w = 0
+    q, dx = _q8(B, K, seed=15)
+    y, _ = gemv_q(64, blocks, q, dx)
+    assert np.all(y == 0.0)
+    y2, isum2 = gemv_q(128, synth.q1_0_blocks(N, K, seed=16), np.zeros((B, K), np.int8),
+                       np.zeros((B, K // 32), np.uint16))
+    assert np.all(y2 == 0.0) and np.all(isum2 == 0)
+
+
+@pytest.mark.parametrize("qk,name,N,K", [(128, "gate", 12288, 4096), (128, "down", 4096, 12288),
+                                         (64, "gate", 12288, 4096), (64, "down", 4096, 12288),
+                                         (64, "k", 1024, 4096)])
+def test_qwen3_shapes_sampled(qk, name, N, K):
+    """Full-size Qwen3-8B projections: the whole GEMV runs on the GPU, sampled rows are compared
+    with the oracle."""
+    blocks = (synth.q1_0_blocks(N, K, seed=500 + N) if qk == 128
+              else synth.q2_0_blocks(N, K, seed=500 + N))
+    q, dx = _q8(1, K, seed=501)
+    y, isum = gemv_q(qk, blocks, q, dx)
+    rows = np.unique(np.concatenate([np.arange(0, N, N // 97), [N - 1]]))
+    ref = (oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product)(blocks[rows], q, dx)
+    assert np.array_equal(isum[:, rows], ref.isum)
+    assert within(y[:, rows], ref.y_exact, ref.mag)[0]
+
+
+# ----------------------------------------------------------------------------------------------
+# planar ternary
+# ----------------------------------------------------------------------------------------------
+def _check_trit(planes, w_scale, q, xs):
+    acc_ref, y_ref = oracle.trit_planes_product(planes, w_scale, q, xs)
+    acc, y = gemv_trit(planes, w_scale, q, xs)
+    assert np.array_equal(acc, acc_ref)
+    assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32)), "planar y not bit-exact"
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 5, 8])
+def test_trit_ragged(B):
+    N, K = 37, 320 if B % 2 else 4160
+    planes, _ = synth.trit_planes(N, K, seed=600 + B)
+    q = synth.int8_codes(B, K, seed=601)
+    xs = np.abs(synth.activations(1, B, seed=602)[0]) * 0.01 + 1e-3
+    _check_trit(planes, synth.w_scale(603), q, xs)
+
+
+@pytest.mark.parametrize("name,N,K", synth.BITNET_2B4T_PROJ[:2] + synth.BITNET_2B4T_PROJ[4:])
+@pytest.mark.parametrize("B", [1, 8])
+def test_trit_bitnet_shapes(name, N, K, B):
+    """BitNet-2B4T projections, int8 per-token absmax activations (quantized on the GPU)."""
+    planes, _ = synth.trit_planes(N, K, seed=700 + N + K)
+    x = synth.activations(B, K, seed=701)
+    qd = torch.empty((B, K), dtype=torch.int8, device="cuda")
+    sd = torch.empty((B,), dtype=torch.float32, device="cuda")
+    lb.lb_quantize_i8_absmax(dev(x), qd, sd, B, K)
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quantize_i8_absmax(x)
+    assert np.array_equal(host(qd), q_ref)
+    _check_trit(planes, synth.w_scale(702), q_ref, s_ref)
+
+
+def test_trit_minus128_extremes():
+    K = 2560
+    q = np.full((2, K), -128, np.int8)
+    q[1] = synth.int8_codes(1, K, seed=9, extremes=True)[0]
+    allset = np.uint64(0xFFFFFFFFFFFFFFFF)
+    planes = np.zeros((3, K // 64, 2), np.uint64)
+    planes[0, :, 0] = allset                      # every column +1
+    planes[1, :, 1] = allset                      # every column -1
+    planes[2] = synth.trit_planes(1, K, seed=10)[0][0]
+    _check_trit(planes, 0.5, q, np.array([1.0, 0.25], np.float32))
+
+
+# ----------------------------------------------------------------------------------------------
+# bf16 head
+# ----------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("B", [1, 2, 4, 8])
+def test_bf16_ragged(B):
+    N, K = 37, 328 if B % 2 else 2568
+    w = synth.bf16_weights(N, K, seed=800 + B)
+    x = synth.activations(B, K, seed=801)
+    y_ref, mag = oracle.bf16_product(w, x)
+    assert within(gemv_bf16(w, x), y_ref, mag)[0]
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_bf16_head_sampled(B):
+    """BitNet-2B4T dense head 128256 x 2560 bf16: full GEMV on the GPU, sampled rows checked."""
+    N, K = synth.BITNET_HEAD
+    w = synth.bf16_weights(N, K, seed=900)
+    x = synth.activations(B, K, seed=901)
+    y = gemv_bf16(w, x)
+    rows = np.unique(np.concatenate([np.arange(0, N, 509), [N - 1]]))
+    y_ref, mag = oracle.bf16_product(w[rows], x)
+    assert within(y[:, rows], y_ref, mag)[0]
