@@ -222,13 +222,19 @@ def bf16_product(w: np.ndarray, x: np.ndarray):
     return y, mag
 
 
+def scale_stride(K: int, qk: int) -> int:
+    """Row stride (in entries) of the repacked scale plane: K/QK rounded up to a multiple of 8."""
+    return (K // qk + 7) // 8 * 8
+
+
 def repack(blocks: np.ndarray, K: int, qk: int):
-    """Split [N][K/QK][18] blocks into (bits uint8 [N][K/QK*16], scales uint16 [N][K/QK])."""
+    """Split [N][K/QK][18] blocks into (bits uint8 [N][K/QK*16], scales uint16 [N][S]) with
+    S = scale_stride(K, qk); scale entries past K/QK are zero padding."""
     blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
     N = blocks.shape[0]
     nblk = K // qk
     bits = np.empty((N, nblk * 16), dtype=np.uint8)
-    scales = np.empty((N, nblk), dtype=np.uint16)
+    scales = np.empty((N, scale_stride(K, qk)), dtype=np.uint16)
     _load().oracle_repack(_ptr(blocks), N, nblk, _ptr(bits), _ptr(scales))
     return bits, scales
 

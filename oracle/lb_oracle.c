@@ -358,17 +358,24 @@ ORACLE_API void oracle_bf16_product(const uint16_t *w, const float *x,
 /* ------------------------------------------------------------------------- */
 /* Load-time split of the 18-byte blocks into two planes (the repacked layout  */
 /* consumed by the GPU library):                                               */
-/*   scales[n][blk]           = fp16 d of block (n, blk)                       */
+/*   S = nblk rounded up to a multiple of 8 (scale rows are 16-byte aligned)   */
+/*   scales[n][blk]           = fp16 d of block (n, blk), blk < nblk           */
+/*   scales[n][blk]           = 0 for nblk <= blk < S (padding)                */
 /*   bits[n][blk*16 + i]      = data byte i of block (n, blk), i in 0..15      */
 /* Bit order inside the data bytes is unchanged.                               */
 /* ------------------------------------------------------------------------- */
 ORACLE_API void oracle_repack(const uint8_t *blocks, int64_t N, int64_t nblk,
                               uint8_t *bits, uint16_t *scales)
 {
+    int64_t S = (nblk + 7) / 8 * 8;
     for (int64_t n = 0; n < N; n++) {
-        for (int64_t blk = 0; blk < nblk; blk++) {
+        for (int64_t blk = 0; blk < S; blk++) {
+            if (blk >= nblk) {
+                scales[n * S + blk] = 0;
+                continue;
+            }
             const uint8_t *src = blocks + (n * nblk + blk) * 18;
-            scales[n * nblk + blk] = block_scale_bits(src);
+            scales[n * S + blk] = block_scale_bits(src);
             for (int i = 0; i < 16; i++)
                 bits[(n * nblk + blk) * 16 + i] = src[2 + i];
         }

@@ -373,7 +373,9 @@ def test_repack_split():
     # two rows x two Q1_0 blocks, every byte distinct: scale bytes 0..1, data bytes 2..17
     blocks = (np.arange(2 * 2 * 18, dtype=np.uint16) % 251).astype(np.uint8).reshape(2, 2, 18)
     bits, scales = oracle.repack(blocks, K=256, qk=128)
-    assert scales.tolist() == [[0x0100, 0x1312], [0x2524, 0x3736]]
+    # scale rows are padded to 8 entries (16 bytes) with zeros
+    assert scales.tolist() == [[0x0100, 0x1312, 0, 0, 0, 0, 0, 0],
+                               [0x2524, 0x3736, 0, 0, 0, 0, 0, 0]]
     assert bits[0, :16].tolist() == list(range(2, 18))
     assert bits[0, 16:].tolist() == list(range(20, 36))
     assert bits[1, :16].tolist() == list(range(38, 54))
