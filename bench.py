@@ -4,9 +4,11 @@
 
 Headline workload (the decode GEMV the metric is quoted on): Q2_0_g64 GEMV, 4096 x 4096 weights,
 batch 1, q8_0 activations.  One step = one pass of the decode hot path over one token: q8_0
-quantization of x [1][4096] followed by the GEMV against R = 64 distinct weight matrices (302 MB
-of packed weights, more than the 129 MB L2, so every step streams its weights from HBM).  The
-step's 65 launches are captured once in a CUDA graph and replayed.
+quantization of x [1][4096] followed by the GEMV of that activation against R = 64 distinct
+4096 x 4096 weight matrices (302 MB of packed weights, more than the 129 MB L2, so every step
+streams its weights from HBM), issued as one grouped call (lb_gemv_q2_0_g64_grouped: the 64
+matrices share the activation, like q|k|v or gate|up).  The step is captured once in a CUDA graph
+and replayed.  The same 64 GEMVs issued as 64 single-matrix launches are reported beside it.
 
 value       packed-weight bytes streamed per second (whole job, all ranks), weights resident in HBM
 e2e         the same metric through the public API with the token's activation copied from pinned
@@ -44,6 +46,11 @@ WORKLOAD = "Q2_0_g64 GEMV 4096x4096, batch 1, q8_0 activations (N(0,1)), codes -
 N_ROT = 64
 ROWS_K = 4096
 ROWS_N = 4096
+
+
+def scale_stride(K, qk):
+    """Row stride of the repacked scale plane (K/QK rounded up to a multiple of 8)."""
+    return (K // qk + 7) // 8 * 8
 
 
 def q2_bytes(N, K):
@@ -160,7 +167,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------------
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for name in ("lb_gemv.cu", "lb_common.cuh"):
+    for name in ("lb_stream.cuh", "lb_gemv_q.cu", "lb_common.cuh"):
         with open(os.path.join(ROOT, "bit_matvec_lb_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -244,14 +251,14 @@ def make_q2_weights(N, K, seed, device="cuda"):
     """Random Q2_0_g64 weights in the repacked layout (code plane + fp16 scale plane)."""
     import synth
     codes = synth.device_q2_codes_packed(N * K // 4, seed, device=device)
-    scales = synth.device_fp16_scales(N * K // 64, seed + 7919, device=device)
+    scales = synth.device_fp16_scales(N * scale_stride(K, 64), seed + 7919, device=device)
     return codes, scales
 
 
 def make_q1_weights(N, K, seed, device="cuda"):
     import synth
     bits = synth.device_bytes(N * K // 8, seed, device=device)
-    scales = synth.device_fp16_scales(N * K // 128, seed + 7919, device=device)
+    scales = synth.device_fp16_scales(N * scale_stride(K, 128), seed + 7919, device=device)
     return bits, scales
 
 
@@ -271,7 +278,7 @@ def headline(lb, args, dist, out):
         aos[:, 0:2] = aos_scales.view(torch.uint8).view(-1, 2)
         aos[:, 2:] = aos_codes.view(-1, 16)
         codes = torch.empty(N * K // 4, dtype=torch.uint8, device="cuda")
-        scales = torch.empty(N * K // 64, dtype=torch.int16, device="cuda")
+        scales = torch.empty(N * scale_stride(K, 64), dtype=torch.int16, device="cuda")
         lb.lb_repack_q2_0_g64(aos, N, K, codes, scales)
         W.append((codes, scales, aos if r == 0 else None))
     torch.cuda.synchronize()
@@ -281,12 +288,16 @@ def headline(lb, args, dist, out):
     d = torch.empty((1, K // 32), dtype=torch.int16, device="cuda")
     Y = torch.empty((N_ROT, 1, N), dtype=torch.float32, device="cuda")
 
+    group = [(W[r][0], W[r][1], Y[r], None, N) for r in range(N_ROT)]
+
     def step():
         lb.lb_quantize_q8_0(x, q, d, 1, K, stream=stream)
-        for r in range(N_ROT):
-            lb.lb_gemv_q2_0_g64(W[r][0], W[r][1], q, d, Y[r], None, N, K, 1, stream=stream)
+        lb.lb_gemv_q2_0_g64_grouped(group, q, d, K, 1, stream=stream)
 
     def gemvs_only():
+        lb.lb_gemv_q2_0_g64_grouped(group, q, d, K, 1, stream=stream)
+
+    def gemvs_single():
         for r in range(N_ROT):
             lb.lb_gemv_q2_0_g64(W[r][0], W[r][1], q, d, Y[r], None, N, K, 1, stream=stream)
 
@@ -326,12 +337,14 @@ def headline(lb, args, dist, out):
     step_bytes = N_ROT * q2_bytes(N, K)
     value = step_bytes * dist.world / (ms * 1e-3) / 1e9
 
-    # ---- roofline: the GEMV alone, average launch duration over the same graph ----
+    # ---- roofline: the grouped GEMV launch alone, average duration over the same graph ----
     hbm, peak_kind = peaks()
-    ms_gemv = time_graph(g_gemv, reps=max(50, args.steps // 4)) / N_ROT
-    alg_bytes = q2_bytes(N, K) + (K + K // 16) + 4 * N      # weights + q8_0 activation + y
+    ms_gemv = time_graph(g_gemv, reps=max(50, args.steps // 4))
+    # weights and scales of 64 matrices + the q8_0 activation + 64 output rows
+    alg_bytes = N_ROT * (q2_bytes(N, K) + 4 * N) + (K + K // 16)
     achieved = alg_bytes / (ms_gemv * 1e-3) / 1e9
-    traffic = profiled_traffic("gemv_q2_0_g64_4096x4096_b1.md")
+    ms_single = time_graph(Graph(gemvs_single, stream), reps=max(20, args.steps // 20)) / N_ROT
+    traffic = profiled_traffic("stream_gemv_q2_0_g64_4096x4096_b1.md")
 
     # ---- e2e: pinned host activation in, outputs out, every step ----
     x_host = torch.from_numpy(x_np).pin_memory()
@@ -359,14 +372,18 @@ def headline(lb, args, dist, out):
         "value": round(value, 2), "ms_per_step": round(ms, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
-                     "peak_kind": peak_kind, "kernel": "gemv_q_kernel<Q2_0_g64, B=1>",
+                     "peak_kind": peak_kind,
+                     "kernel": "stream_gemv_kernel<Q2_0_g64, B=1> (64-matrix grouped launch)",
                      "alg_bytes_per_launch": alg_bytes, "avg_launch_us": round(ms_gemv * 1e3, 3)},
         "e2e": {"value": round(step_bytes * dist.world / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(x_host.numel() * 4),
                 "d2h_bytes_per_step": int(y_host.numel() * 4)},
         "clocks": clocks,
-        "gpu_launches": int(args.steps * (N_ROT + 1)),
+        "gpu_launches": int(args.steps * 2),
         "pct_hbm": round(100 * value / dist.world / hbm, 2),
+        "single_launch": {"GB/s": round(q2_bytes(N, K) / (ms_single * 1e-3) / 1e9, 1),
+                          "us_per_gemv": round(ms_single * 1e3, 3),
+                          "note": "the same 64 GEMVs as 64 single-matrix launches (PDL-chained)"},
     })
 
     if dist.rank == 0:
@@ -399,10 +416,11 @@ def rows_measure(lb, out):
     d = torch.empty((B, K // 32), dtype=torch.int16, device="cuda")
     Y = torch.empty((N_ROT, B, N), dtype=torch.float32, device="cuda")
 
+    group8 = [(W[r][0], W[r][1], Y[r], None, N) for r in range(N_ROT)]
+
     def step_b8():
         lb.lb_quantize_q8_0(x, q, d, B, K, stream=stream)
-        for r in range(N_ROT):
-            lb.lb_gemv_q2_0_g64(W[r][0], W[r][1], q, d, Y[r], None, N, K, B, stream=stream)
+        lb.lb_gemv_q2_0_g64_grouped(group8, q, d, K, B, stream=stream)
     ms = time_graph(Graph(step_b8, stream), reps=50)
     gbs = N_ROT * q2_bytes(N, K) / (ms * 1e-3) / 1e9
     rows["q2_0_g64_4096x4096_b8"] = {"GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
@@ -413,7 +431,8 @@ def rows_measure(lb, out):
     # (2) Qwen3-8B-shaped decode token, Q1_0 and Q2_0_g64, batch 1 (252 GEMVs, 36 layers)
     for fmt in ("q2_0_g64", "q1_0"):
         make = make_q2_weights if fmt == "q2_0_g64" else make_q1_weights
-        gemv = lb.lb_gemv_q2_0_g64 if fmt == "q2_0_g64" else lb.lb_gemv_q1_0
+        grouped = (lb.lb_gemv_q2_0_g64_grouped if fmt == "q2_0_g64"
+                   else lb.lb_gemv_q1_0_grouped)
         nbytes = q2_bytes if fmt == "q2_0_g64" else q1_bytes
         layers = []
         total = 0
@@ -426,19 +445,24 @@ def rows_measure(lb, out):
         xs = {k: torch.from_numpy(synth.activations(1, k, seed=k)).cuda() for k in (4096, 12288)}
         qs = {k: torch.empty((1, k), dtype=torch.int8, device="cuda") for k in (4096, 12288)}
         ds = {k: torch.empty((1, k // 32), dtype=torch.int16, device="cuda") for k in (4096, 12288)}
-        ybuf = torch.empty(12288, dtype=torch.float32, device="cuda")
+        ybufs = [torch.empty(12288, dtype=torch.float32, device="cuda") for _ in range(7)]
+        # q|k|v and gate|up read the same activation: one grouped call each
+        groups = [(0, 1, 2), (3,), (4, 5), (6,)]
 
         def token():
             for proj in layers:
-                for i, ((w, s), n, k) in enumerate(proj):
-                    if i in (0, 3, 6):   # new activation: attention input, attention output, FFN
+                for gi, members in enumerate(groups):
+                    k = proj[members[0]][2]
+                    if gi in (0, 1, 3):  # new activation: attention input, attention out, FFN
                         lb.lb_quantize_q8_0(xs[k], qs[k], ds[k], 1, k, stream=stream)
-                    gemv(w, s, qs[k], ds[k], ybuf, None, n, k, 1, stream=stream)
+                    mats = [(proj[i][0][0], proj[i][0][1], ybufs[i], None, proj[i][1])
+                            for i in members]
+                    grouped(mats, qs[k], ds[k], k, 1, stream=stream)
         ms = time_graph(Graph(token, stream), reps=20)
         gbs = total / (ms * 1e-3) / 1e9
         rows[f"qwen3_8b_token_{fmt}_b1"] = {"GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
                                             "ms_per_token": round(ms, 4), "bytes": total,
-                                            "launches": 36 * 10}
+                                            "launches": 36 * 7}
         del layers
         torch.cuda.empty_cache()
 
@@ -458,17 +482,22 @@ def rows_measure(lb, out):
         xq = {k: (torch.empty((B, k), dtype=torch.int8, device="cuda"),
                   torch.empty((B,), dtype=torch.float32, device="cuda")) for k in (2560, 6912)}
         xh = torch.from_numpy(synth.activations(B, HK, seed=3)).cuda()
-        yb = torch.empty((B, 6912), dtype=torch.float32, device="cuda")
+        ybs = [torch.empty((B, 6912), dtype=torch.float32, device="cuda") for _ in range(7)]
         yh = torch.empty((B, HN), dtype=torch.float32, device="cuda")
         x2560 = x[:, :2560].contiguous()
+        groups = [(0, 1, 2), (3,), (4, 5), (6,)]
 
         def token_bitnet():
-            for i, (planes, n, k) in enumerate(body):
-                if i % 7 in (0, 3, 6):
-                    src = x2560 if k == 2560 else x
-                    lb.lb_quantize_i8_absmax(src, xq[k][0], xq[k][1], B, k, stream=stream)
-                lb.lb_gemv_trit_planes(planes, 0.02, xq[k][0], xq[k][1], yb, None, n, k, B,
-                                       stream=stream)
+            for layer in range(synth.BITNET_2B4T_LAYERS):
+                proj = body[7 * layer: 7 * layer + 7]
+                for gi, members in enumerate(groups):
+                    k = proj[members[0]][2]
+                    if gi in (0, 1, 3):
+                        src = x2560 if k == 2560 else x
+                        lb.lb_quantize_i8_absmax(src, xq[k][0], xq[k][1], B, k, stream=stream)
+                    mats = [(proj[i][0], 0.02, ybs[i], None, proj[i][1]) for i in members]
+                    lb.lb_gemv_trit_planes_grouped(mats, xq[k][0], xq[k][1], k, B,
+                                                   stream=stream)
             lb.lb_gemv_bf16(head, xh, yh, HN, HK, B, stream=stream)
 
         def head_only():

@@ -15,9 +15,10 @@ import threading
 from . import build as _build
 
 __all__ = [
-    "LBError", "load", "library_path", "status_string",
+    "LBError", "load", "library_path", "status_string", "scale_stride", "lb_device_status",
     "lb_quantize_q8_0", "lb_quantize_i8_absmax", "lb_repack_q1_0", "lb_repack_q2_0_g64",
     "lb_gemv_q1_0", "lb_gemv_q2_0_g64", "lb_gemv_trit_planes", "lb_gemv_bf16",
+    "lb_gemv_q1_0_grouped", "lb_gemv_q2_0_g64_grouped", "lb_gemv_trit_planes_grouped",
 ]
 
 LB_STATUS = {0: "LB_OK", -1: "LB_ERR_NULL", -2: "LB_ERR_ALIGN", -3: "LB_ERR_SHAPE",
@@ -37,6 +38,17 @@ I64 = ctypes.c_int64
 I32 = ctypes.c_int
 F32 = ctypes.c_float
 
+MAX_GROUP = 64
+
+
+class lb_q_matrix(ctypes.Structure):
+    _fields_ = [("bits", P), ("scales", P), ("y", P), ("isum_opt", P), ("N", I64)]
+
+
+class lb_trit_matrix(ctypes.Structure):
+    _fields_ = [("planes", P), ("w_scale", F32), ("y", P), ("acc_opt", P), ("N", I64)]
+
+
 SIGNATURES = {
     "lb_status_string": (ctypes.c_char_p, [I32]),
     "lb_version": (I32, []),
@@ -48,6 +60,11 @@ SIGNATURES = {
     "lb_gemv_q2_0_g64": (I32, [P, P, P, P, P, P, I64, I64, I32, P]),
     "lb_gemv_trit_planes": (I32, [P, F32, P, P, P, P, I64, I64, I32, P]),
     "lb_gemv_bf16": (I32, [P, P, P, I64, I64, I32, P]),
+    "lb_device_status": (I32, [P]),
+    "lb_gemv_q1_0_grouped": (I32, [ctypes.POINTER(lb_q_matrix), I32, P, P, I64, I32, P]),
+    "lb_gemv_q2_0_g64_grouped": (I32, [ctypes.POINTER(lb_q_matrix), I32, P, P, I64, I32, P]),
+    "lb_gemv_trit_planes_grouped": (I32, [ctypes.POINTER(lb_trit_matrix), I32, P, P, I64, I32,
+                                          P]),
 }
 
 
@@ -72,6 +89,11 @@ def load(build_if_missing: bool = True):
                 fn.argtypes = args
             _lib = lib
     return _lib
+
+
+def scale_stride(K: int, qk: int) -> int:
+    """Row stride (entries) of a repacked scale plane: K/QK rounded up to a multiple of 8."""
+    return (K // qk + 7) // 8 * 8
 
 
 def status_string(status: int) -> str:
@@ -147,3 +169,42 @@ def lb_gemv_trit_planes(planes, w_scale: float, q, x_scale, y, acc, N: int, K: i
 def lb_gemv_bf16(w, x, y, N: int, K: int, B: int, stream=None):
     _check("lb_gemv_bf16", load().lb_gemv_bf16(_ptr(w), _ptr(x), _ptr(y), N, K, B,
                                                _stream(stream)))
+
+
+def lb_device_status(stream=None) -> int:
+    """Synchronize the stream and return (and clear) the device error status (0 = OK)."""
+    return load().lb_device_status(_stream(stream))
+
+
+def _q_mats(mats):
+    if not 1 <= len(mats) <= MAX_GROUP:
+        raise ValueError(f"a group holds 1..{MAX_GROUP} matrices")
+    arr = (lb_q_matrix * len(mats))()
+    for i, (bits, scales, y, isum, N) in enumerate(mats):
+        arr[i] = lb_q_matrix(_ptr(bits), _ptr(scales), _ptr(y), _ptr(isum), int(N))
+    return arr
+
+
+def lb_gemv_q1_0_grouped(mats, q, d, K: int, B: int, stream=None):
+    """mats: sequence of (bits, scales, y, isum_or_None, N) sharing the activation q, d."""
+    arr = _q_mats(mats)
+    _check("lb_gemv_q1_0_grouped", load().lb_gemv_q1_0_grouped(
+        arr, len(mats), _ptr(q), _ptr(d), K, B, _stream(stream)))
+
+
+def lb_gemv_q2_0_g64_grouped(mats, q, d, K: int, B: int, stream=None):
+    """mats: sequence of (codes, scales, y, isum_or_None, N) sharing the activation q, d."""
+    arr = _q_mats(mats)
+    _check("lb_gemv_q2_0_g64_grouped", load().lb_gemv_q2_0_g64_grouped(
+        arr, len(mats), _ptr(q), _ptr(d), K, B, _stream(stream)))
+
+
+def lb_gemv_trit_planes_grouped(mats, q, x_scale, K: int, B: int, stream=None):
+    """mats: sequence of (planes, w_scale, y, acc_or_None, N) sharing the activation."""
+    if not 1 <= len(mats) <= MAX_GROUP:
+        raise ValueError(f"a group holds 1..{MAX_GROUP} matrices")
+    arr = (lb_trit_matrix * len(mats))()
+    for i, (planes, w_scale, y, acc, N) in enumerate(mats):
+        arr[i] = lb_trit_matrix(_ptr(planes), float(w_scale), _ptr(y), _ptr(acc), int(N))
+    _check("lb_gemv_trit_planes_grouped", load().lb_gemv_trit_planes_grouped(
+        arr, len(mats), _ptr(q), _ptr(x_scale), K, B, _stream(stream)))

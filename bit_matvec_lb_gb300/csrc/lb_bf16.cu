@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kBfThreads)
                      float *__restrict__ y, int64_t N, int64_t K) {
     extern __shared__ float4 xs[];  // [B][K/4] float4, swizzled in pairs
     const int64_t nchunk = K / 8;
+    pdl_launch_dependents();
+    pdl_wait();
     for (int64_t i = threadIdx.x; i < (int64_t)B * nchunk * 2; i += blockDim.x) {
         const int64_t b = i / (nchunk * 2), rem = i % (nchunk * 2);
         const int64_t c = rem >> 1;
@@ -91,8 +93,7 @@ static int launch_bf16(const uint16_t *w, const float *x, float *y, int64_t N, i
     int64_t want = ((N + R - 1) / R + kBfWarps - 1) / kBfWarps;
     int64_t cap = (int64_t)sms * bps;
     int grid = (int)(want < cap ? (want < 1 ? 1 : want) : cap);
-    kern<<<grid, kBfThreads, smem, st>>>(w, x, y, N, K);
-    return launch_status();
+    return launch_pdl(kern, dim3(grid), dim3(kBfThreads), smem, st, w, x, y, N, K);
 }
 
 }  // namespace lb

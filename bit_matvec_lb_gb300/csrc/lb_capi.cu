@@ -1,4 +1,5 @@
-// lb_capi.cu -- status names, version, and the device check shared by every entry point.
+// lb_capi.cu -- status names, version, device status, and the host helpers shared by every
+// entry point (device check, error word, cached kernel preparation).
 //
 // Calls refuse with a reason and never fall back to another path: a device that is not
 // compute capability 10.3 gets LB_ERR_ARCH (the pages' rule for kernel selection is the same:
@@ -40,6 +41,25 @@ int current_device_info(DeviceInfo *out) {
         *out = g_info[dev];
     }
     return out->ok == 1 ? LB_OK : LB_ERR_ARCH;
+}
+
+// One error word per device (file-scope device variable; the host passes its address).
+__device__ int g_device_error;
+static int *g_err_addr[kMaxDevices];
+
+int *device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_info_mutex);
+    if (!g_err_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_err_addr[dev] = static_cast<int *>(p);
+    }
+    return g_err_addr[dev];
 }
 
 struct KernelPrep {
@@ -97,3 +117,18 @@ LB_EXPORT const char *lb_status_string(int status) {
 }
 
 LB_EXPORT int lb_version(void) { return 100; }
+
+LB_EXPORT int lb_device_status(void *stream) {
+    using namespace lb;
+    DeviceInfo di;
+    if (int st = current_device_info(&di)) return st;
+    int *word = device_error_word();
+    if (!word) return LB_ERR_LAUNCH;
+    int host = 0;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(&host, word, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(word, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return LB_ERR_LAUNCH;
+    return host == 0 ? LB_OK : LB_ERR_DEVICE;
+}

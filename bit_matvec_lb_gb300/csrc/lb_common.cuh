@@ -24,12 +24,35 @@ struct DeviceInfo {
 
 int current_device_info(DeviceInfo *out);  // LB_OK or LB_ERR_ARCH
 
-inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+// Address (device pointer) of the current device's error word: kernels that give up on a
+// bounded wait set it; lb_device_status() reads and clears it.
+int *device_error_word();
 
 // Per-kernel launch preparation, cached: raise the dynamic shared-memory limit once and
-// remember the occupancy for the last shared-memory size used.  LB_OK, or LB_ERR_SHAPE when
-// the requested shared memory cannot be resident, or LB_ERR_LAUNCH.
+// remember the occupancy for the last shared-memory size used.  LB_OK, LB_ERR_SHAPE when the
+// requested shared memory cannot be resident, or LB_ERR_LAUNCH.
 int prepare_kernel(const void *kernel, int threads, size_t smem, int *blocks_per_sm);
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Launch `kernel` with programmatic stream serialization allowed (see pdl_wait()).
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess
+               ? LB_OK
+               : LB_ERR_LAUNCH;
+}
 
 inline int launch_status() {
     cudaError_t e = cudaPeekAtLastError();
@@ -88,5 +111,83 @@ __device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t 
 }
 
 __device__ __forceinline__ int byte_sum_s8(uint32_t w) { return dp4a_ss(w, 0x01010101u, 0); }
+
+// Programmatic dependent launch.  Every kernel of the library is launched so that the next
+// kernel in the stream may start once all of its CTAs have called pdl_launch_dependents(); each
+// kernel calls pdl_wait() -- which returns when the previous kernel in the stream has completed
+// and its memory is visible -- before it reads or writes any buffer another kernel may touch.
+// Only reads of weights happen before pdl_wait().  The one kernel of the library that writes
+// weights (the load-time repack) never triggers early, so a kernel launched after it starts
+// only once it has completed; kernels of other libraries (torch, copies) never trigger early
+// either.  Without a programmatic predecessor both instructions are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA, non-tensor) primitives, CTA scope.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait on the phase with the given parity: true once it completes, false after about
+// `limit_ns` (the caller then reports through the error word and stops instead of hanging).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; i++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
+}
+// Bulk copy global -> this CTA's shared memory; completion is counted on `bar` (tx bytes).
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Named barrier over `count` threads (id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 }  // namespace lb

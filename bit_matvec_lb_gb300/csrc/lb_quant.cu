@@ -14,6 +14,8 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__rest
                                                             uint32_t *__restrict__ q,
                                                             uint16_t *__restrict__ d,
                                                             int64_t nquads) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int lane = threadIdx.x & 31;
     // The loop condition is warp-uniform so every lane reaches the shuffles; nquads is a
@@ -47,6 +49,8 @@ __global__ void __launch_bounds__(512) quantize_i8_absmax_kernel(const float *__
                                                                  float *__restrict__ x_scale,
                                                                  int64_t K) {
     __shared__ float red[32];
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t b = blockIdx.x;
     const float4 *xb = reinterpret_cast<const float4 *>(x + b * K);
     const int64_t nq = K / 4;
@@ -82,21 +86,32 @@ __global__ void __launch_bounds__(512) quantize_i8_absmax_kernel(const float *__
     }
 }
 
-// One thread per 18-byte source block: fp16 scale to `scales`, 16 data bytes to `bits`.
+// One thread per scale slot (n, j), j < S: block j of row n when j < nblk (fp16 scale to
+// `scales`, 16 data bytes to `bits`), a zero padding scale otherwise.
 __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ blocks,
                                                      uint4 *__restrict__ bits,
-                                                     uint16_t *__restrict__ scales,
-                                                     int64_t nblocks) {
+                                                     uint16_t *__restrict__ scales, int64_t N,
+                                                     int64_t nblk, int64_t S) {
+    // No early trigger here: repack WRITES weights, and the GEMVs read weights before their
+    // grid-dependency wait, so a kernel launched after a repack must start only once the repack
+    // has completed.
+    pdl_wait();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks; i += stride) {
-        const uint8_t *src = blocks + i * 18;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < N * S; i += stride) {
+        const int64_t n = i / S, j = i % S;
+        if (j >= nblk) {
+            scales[i] = 0;
+            continue;
+        }
+        const int64_t b = n * nblk + j;
+        const uint8_t *src = blocks + b * 18;
         scales[i] = (uint16_t)(src[0] | ((uint16_t)src[1] << 8));
         uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 4; j++)
-            w[j] = (uint32_t)src[2 + 4 * j] | ((uint32_t)src[3 + 4 * j] << 8) |
-                   ((uint32_t)src[4 + 4 * j] << 16) | ((uint32_t)src[5 + 4 * j] << 24);
-        bits[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int k = 0; k < 4; k++)
+            w[k] = (uint32_t)src[2 + 4 * k] | ((uint32_t)src[3 + 4 * k] << 8) |
+                   ((uint32_t)src[4 + 4 * k] << 16) | ((uint32_t)src[5 + 4 * k] << 24);
+        bits[b] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -120,9 +135,9 @@ LB_EXPORT int lb_quantize_q8_0(const float *x, int8_t *q, uint16_t *d, int64_t B
     DeviceInfo di;
     if (int st = current_device_info(&di)) return st;
     const int64_t nquads = B * K / 4;
-    quantize_q8_0_kernel<<<grid_for(nquads, 256, di.sms), 256, 0, as_stream(stream)>>>(
-        reinterpret_cast<const float4 *>(x), reinterpret_cast<uint32_t *>(q), d, nquads);
-    return launch_status();
+    return launch_pdl(quantize_q8_0_kernel, dim3(grid_for(nquads, 256, di.sms)), dim3(256), 0,
+                      as_stream(stream), reinterpret_cast<const float4 *>(x),
+                      reinterpret_cast<uint32_t *>(q), d, nquads);
 }
 
 LB_EXPORT int lb_quantize_i8_absmax(const float *x, int8_t *q, float *x_scale, int64_t B,
@@ -132,8 +147,8 @@ LB_EXPORT int lb_quantize_i8_absmax(const float *x, int8_t *q, float *x_scale, i
     if (B < 1 || B > 0x7fffffff || K < 16 || K % 16 != 0) return LB_ERR_SHAPE;
     DeviceInfo di;
     if (int st = current_device_info(&di)) return st;
-    quantize_i8_absmax_kernel<<<(unsigned)B, 512, 0, as_stream(stream)>>>(x, q, x_scale, K);
-    return launch_status();
+    return launch_pdl(quantize_i8_absmax_kernel, dim3((unsigned)B), dim3(512), 0,
+                      as_stream(stream), x, q, x_scale, K);
 }
 
 static int repack_common(const void *blocks18, int64_t N, int64_t K, int qk, uint8_t *bits,
@@ -143,11 +158,10 @@ static int repack_common(const void *blocks18, int64_t N, int64_t K, int qk, uin
     if (N < 1 || K < qk || K % qk != 0) return LB_ERR_SHAPE;
     DeviceInfo di;
     if (int st = current_device_info(&di)) return st;
-    const int64_t nblocks = N * (K / qk);
-    repack_kernel<<<grid_for(nblocks, 256, di.sms), 256, 0, as_stream(stream)>>>(
-        reinterpret_cast<const uint8_t *>(blocks18), reinterpret_cast<uint4 *>(bits), scales,
-        nblocks);
-    return launch_status();
+    const int64_t nblk = K / qk, S = (nblk + 7) / 8 * 8;
+    return launch_pdl(repack_kernel, dim3(grid_for(N * S, 256, di.sms)), dim3(256), 0,
+                      as_stream(stream), reinterpret_cast<const uint8_t *>(blocks18),
+                      reinterpret_cast<uint4 *>(bits), scales, N, nblk, S);
 }
 
 LB_EXPORT int lb_repack_q1_0(const void *blocks18, int64_t N, int64_t K, uint8_t *bits,

@@ -31,6 +31,11 @@
  *     path: a device that is not sm_103 is refused with LB_ERR_ARCH.
  *   - Inputs must be finite; NaN or Inf activations give unspecified (but in-bounds) results.
  *   - Calls that write the same output buffer must not overlap on the GPU.
+ *   - Kernels are launched with programmatic dependent launch: a GEMV may start streaming its
+ *     WEIGHTS while the previous kernel of this library in the stream is still finishing, and
+ *     waits for that kernel before touching activations or outputs.  lb_repack_* (the only call
+ *     that writes weights) always completes before the next kernel starts; weights written by
+ *     other code are read only after that code's kernels have completed.
  */
 #ifndef LB_H_
 #define LB_H_
@@ -48,13 +53,18 @@ extern "C" {
 #define LB_ERR_BATCH (-4)   /* GEMV batch outside [1, 8] */
 #define LB_ERR_ARCH (-5)    /* the current device is not compute capability 10.3 */
 #define LB_ERR_LAUNCH (-6)  /* the CUDA launch failed (the CUDA error is left pending) */
-#define LB_ERR_DEVICE (-7)  /* a device-side check failed (reported through dev_err) */
+#define LB_ERR_DEVICE (-7)  /* a kernel gave up on a bounded wait (see lb_device_status) */
 
 /* Name of a status code ("LB_OK", "LB_ERR_SHAPE", ...); never NULL. */
 const char *lb_status_string(int status);
 
 /* Library version as 10000*major + 100*minor + patch. */
 int lb_version(void);
+
+/* Synchronizes `stream`, then reads and clears the current device's error word.  Returns LB_OK,
+ * or LB_ERR_DEVICE if a kernel of this library gave up on a bounded wait since the last call
+ * (its outputs are then incomplete).  Kernels never hang: every wait gives up after about 2 s. */
+int lb_device_status(void *stream);
 
 /* ---------------------------------------------------------------------------------------
  * Activation quantizers
@@ -82,9 +92,12 @@ int lb_quantize_i8_absmax(const float *x, int8_t *q, float *x_scale, int64_t B, 
  *   blocks18 : [N][K/QK][18] source bytes (fp16 d little-endian, then 16 data bytes);
  *              QK = 128 for Q1_0, 64 for Q2_0_g64. This pointer needs no alignment.
  *   bits     : [N][K/QK * 16] data bytes, bit order unchanged.
- *   scales   : [N][K/QK] fp16 bit patterns.
+ *   scales   : [N][S] fp16 bit patterns, S = LB_SCALE_STRIDE(K, QK) = K/QK rounded up to a
+ *              multiple of 8, so every row of scales is 16-byte aligned; the S - K/QK padding
+ *              entries of each row are written as 0.
  * Q1_0: K % 128 == 0. Q2_0_g64: K % 64 == 0. N >= 1.
  * ------------------------------------------------------------------------------------- */
+#define LB_SCALE_STRIDE(K, QK) ((((K) / (QK)) + 7) / 8 * 8)
 int lb_repack_q1_0(const void *blocks18, int64_t N, int64_t K, uint8_t *bits, uint16_t *scales,
                    void *stream);
 int lb_repack_q2_0_g64(const void *blocks18, int64_t N, int64_t K, uint8_t *codes,
@@ -92,13 +105,39 @@ int lb_repack_q2_0_g64(const void *blocks18, int64_t N, int64_t K, uint8_t *code
 
 /* ---------------------------------------------------------------------------------------
  * Decode GEMVs (batch B in [1, 8] tokens sharing the weights)
+ *
+ * Every GEMV exists in a single-matrix form and a grouped form.  The grouped form computes the
+ * products of up to LB_MAX_GROUP weight matrices with the SAME activation in one launch (for
+ * example the q, k and v projections, or gate and up), which amortizes the launch over all of
+ * them; each matrix has its own rows N, weights and output.  The descriptor array is read on the
+ * host during the call (it may be freed on return).  Output buffers must not overlap.
+ * Shared memory bounds the activation: B * K * 1.25 bytes must stay below about 120 KB
+ * (LB_ERR_SHAPE otherwise).
  * ------------------------------------------------------------------------------------- */
+#define LB_MAX_GROUP 64
+
+typedef struct lb_q_matrix {
+    const uint8_t *bits;     /* [N][K/QK*16] repacked sign bytes (Q1_0) or code bytes (Q2_0_g64) */
+    const uint16_t *scales;  /* [N][LB_SCALE_STRIDE(K, QK)] fp16 scales */
+    float *y;                /* [B][N] fp32 output */
+    int32_t *isum_opt;       /* NULL, or [B][N][K/32] int32 block sums (test hook) */
+    int64_t N;               /* rows, 1 <= N <= 2^30 */
+} lb_q_matrix;
+
+typedef struct lb_trit_matrix {
+    const uint64_t *planes;  /* [N][K/64][2] {pos, neg} beats */
+    float w_scale;           /* per-tensor weight scale */
+    float *y;                /* [B][N] fp32 output */
+    int32_t *acc_opt;        /* NULL, or [B][N] int32 accumulators */
+    int64_t N;               /* rows, 1 <= N <= 2^30 */
+} lb_trit_matrix;
 
 /* Q1_0 x q8_0 ([TR] III.2-III.3). For token b, row n, weight block k (128 weights) and its
  * four q8_0 blocks j:
  *   isum_j = sum_{i in j} s_i * q_i  (s_i = +1 for a set bit, -1 otherwise; integer, exact)
  *   y[b][n] = sum_k d_w[n][k] * sum_j d_x[b][j] * isum_j      (fp32 accumulation)
- *   bits   : [N][K/8] repacked sign bytes (lb_repack_q1_0).   scales : [N][K/128] fp16.
+ *   bits   : [N][K/8] repacked sign bytes (lb_repack_q1_0).
+ *   scales : [N][LB_SCALE_STRIDE(K, 128)] fp16 (lb_repack_q1_0).
  *   q, d   : q8_0 activations [B][K] int8, [B][K/32] fp16 (lb_quantize_q8_0 layout).
  *   y      : [B][N] fp32.
  *   isum_opt : NULL, or [B][N][K/32] int32 that receives every isum_j (a test hook; the same
@@ -109,14 +148,24 @@ int lb_gemv_q1_0(const uint8_t *bits, const uint16_t *scales, const int8_t *q,
                  const uint16_t *d, float *y, int32_t *isum_opt, int64_t N, int64_t K, int B,
                  void *stream);
 
+/* Grouped Q1_0 GEMV: mats[0..G-1] (host array, 1 <= G <= LB_MAX_GROUP) against one q8_0
+ * activation q, d of B tokens and K columns; same arithmetic and limits as lb_gemv_q1_0. */
+int lb_gemv_q1_0_grouped(const lb_q_matrix *mats, int G, const int8_t *q, const uint16_t *d,
+                         int64_t K, int B, void *stream);
+
 /* Q2_0_g64 x q8_0 ([TR] III.5, III.8): as lb_gemv_q1_0 with 64-weight blocks, weight i of a
  * block = ((codes byte i/4) >> 2*(i%4)) & 3, minus 1, in {-1, 0, +1, +2}, and two q8_0
  * blocks per weight block.
- *   codes : [N][K/4] repacked code bytes (lb_repack_q2_0_g64).   scales : [N][K/64] fp16.
+ *   codes : [N][K/4] repacked code bytes (lb_repack_q2_0_g64).
+ *   scales : [N][LB_SCALE_STRIDE(K, 64)] fp16.
  * K % 64 == 0; N >= 1; B in [1, 8]. */
 int lb_gemv_q2_0_g64(const uint8_t *codes, const uint16_t *scales, const int8_t *q,
                      const uint16_t *d, float *y, int32_t *isum_opt, int64_t N, int64_t K,
                      int B, void *stream);
+
+/* Grouped Q2_0_g64 GEMV (see lb_gemv_q1_0_grouped). */
+int lb_gemv_q2_0_g64_grouped(const lb_q_matrix *mats, int G, const int8_t *q, const uint16_t *d,
+                             int64_t K, int B, void *stream);
 
 /* Planar ternary select-accumulate ([TA] 1, 2, 4.1, 5):
  *   acc[b][r] = sum_{c: pos bit set} q[b][c] - sum_{c: neg bit set} q[b][c]   (int32, exact,
@@ -130,6 +179,10 @@ int lb_gemv_q2_0_g64(const uint8_t *codes, const uint16_t *scales, const int8_t 
 int lb_gemv_trit_planes(const uint64_t *planes, float w_scale, const int8_t *q,
                         const float *x_scale, float *y, int32_t *acc_opt, int64_t N, int64_t K,
                         int B, void *stream);
+
+/* Grouped planar GEMV: mats[0..G-1] (host array) against one activation q, x_scale. */
+int lb_gemv_trit_planes_grouped(const lb_trit_matrix *mats, int G, const int8_t *q,
+                                const float *x_scale, int64_t K, int B, void *stream);
 
 /* Dense bf16 head ([TA] 3): y[b][n] = sum_k float(W[n][k]) * x[b][k], fp32 accumulation,
  * bf16 widened exactly (16-bit left shift).

@@ -20,11 +20,15 @@ def host(t: torch.Tensor, dtype=None) -> np.ndarray:
     return a.view(dtype) if dtype is not None else a
 
 
+def scale_stride(K: int, qk: int) -> int:
+    return (K // qk + 7) // 8 * 8
+
+
 def repack_on_gpu(blocks: np.ndarray, K: int, qk: int):
     N = blocks.shape[0]
     src = dev(blocks.reshape(-1))
     bits = torch.empty(N * (K // qk) * 16, dtype=torch.uint8, device="cuda")
-    scales = torch.empty(N * (K // qk), dtype=torch.int16, device="cuda")
+    scales = torch.full((N * scale_stride(K, qk),), 0x7FFF, dtype=torch.int16, device="cuda")
     fn = lb.lb_repack_q1_0 if qk == 128 else lb.lb_repack_q2_0_g64
     fn(src, N, K, bits, scales)
     return bits, scales

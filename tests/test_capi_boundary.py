@@ -116,3 +116,25 @@ def test_python_binding_raises_on_error():
     with pytest.raises(lb.LBError) as e:
         lb.lb_gemv_bf16(A, A, A, 4, 12, 1, stream=0)
     assert e.value.status == -3 and "LB_ERR_SHAPE" in str(e.value)
+
+
+def test_grouped_refusals(lib):
+    arr = (lb.lb_q_matrix * 2)()
+    arr[0] = lb.lb_q_matrix(A, A, A, None, 4)
+    arr[1] = lb.lb_q_matrix(A, A, A, None, 4)
+    assert lib.lb_gemv_q2_0_g64_grouped(arr, 0, A, A, 64, 1, None) == -3      # empty group
+    assert lib.lb_gemv_q2_0_g64_grouped(arr, 65, A, A, 64, 1, None) == -3     # too many
+    arr[1] = lb.lb_q_matrix(A, None, A, None, 4)
+    assert lib.lb_gemv_q2_0_g64_grouped(arr, 2, A, A, 64, 1, None) == -1      # NULL scales
+    arr[1] = lb.lb_q_matrix(A, A, MIS, None, 4)
+    assert lib.lb_gemv_q1_0_grouped(arr, 2, A, A, 128, 1, None) == -2         # misaligned y
+    arr[1] = lb.lb_q_matrix(A, A, A, None, 0)
+    assert lib.lb_gemv_q1_0_grouped(arr, 2, A, A, 128, 1, None) == -3         # N = 0
+    t = (lb.lb_trit_matrix * 1)()
+    t[0] = lb.lb_trit_matrix(A, 1.0, A, None, 4)
+    assert lib.lb_gemv_trit_planes_grouped(t, 1, A, A, 64, 9, None) == -4
+
+
+def test_scale_stride():
+    assert lb.scale_stride(512, 128) == 8 and lb.scale_stride(4096, 64) == 64
+    assert lb.scale_stride(4224, 128) == 40 and lb.scale_stride(320, 64) == 8

@@ -260,3 +260,88 @@ def test_bf16_head_sampled(B):
     rows = np.unique(np.concatenate([np.arange(0, N, 509), [N - 1]]))
     y_ref, mag = oracle.bf16_product(w[rows], x)
     assert within(y[:, rows], y_ref, mag)[0]
+
+
+# ----------------------------------------------------------------------------------------------
+# grouped GEMVs: several matrices sharing one activation in one launch
+# ----------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("qk", [128, 64])
+@pytest.mark.parametrize("B", [1, 2, 5, 8])
+def test_grouped_q(qk, B):
+    K = 1280 if qk == 128 else 1088
+    Ns = [300, 77, 77, 9, 1, 130]
+    make = synth.q1_0_blocks if qk == 128 else synth.q2_0_blocks
+    blocks = [make(n, K, seed=1000 + i) for i, n in enumerate(Ns)]
+    q, dx = _q8(B, K, seed=1100 + B)
+    mats, outs = [], []
+    for i, (n, bl) in enumerate(zip(Ns, blocks)):
+        bits, scales = repack_on_gpu(bl, K, qk)
+        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
+        isum = torch.empty((B, n, K // 32), dtype=torch.int32, device="cuda") if i % 2 else None
+        mats.append((bits, scales, y, isum, n))
+        outs.append((y, isum))
+    fn = lb.lb_gemv_q1_0_grouped if qk == 128 else lb.lb_gemv_q2_0_g64_grouped
+    fn(mats, dev(q), dev(dx), K, B)
+    torch.cuda.synchronize()
+    ref_fn = oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product
+    for bl, (y, isum) in zip(blocks, outs):
+        ref = ref_fn(bl, q, dx)
+        assert within(host(y), ref.y_exact, ref.mag)[0]
+        if isum is not None:
+            assert np.array_equal(host(isum), ref.isum)
+    assert lb.lb_device_status() == 0
+
+
+def test_grouped_q2_full_group():
+    """LB_MAX_GROUP matrices in one launch (tile indexing across the whole group)."""
+    K, B = 512, 1
+    Ns = [17 + (i * 37) % 90 for i in range(lb.MAX_GROUP)]
+    blocks = [synth.q2_0_blocks(n, K, seed=2000 + i) for i, n in enumerate(Ns)]
+    q, dx = _q8(B, K, seed=2100)
+    mats, ys = [], []
+    for n, bl in zip(Ns, blocks):
+        bits, scales = repack_on_gpu(bl, K, 64)
+        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
+        mats.append((bits, scales, y, None, n))
+        ys.append(y)
+    lb.lb_gemv_q2_0_g64_grouped(mats, dev(q), dev(dx), K, B)
+    torch.cuda.synchronize()
+    for bl, y in zip(blocks, ys):
+        ref = oracle.q2_0_g64_product(bl, q, dx, want_isum=False)
+        assert within(host(y), ref.y_exact, ref.mag)[0]
+
+
+@pytest.mark.parametrize("qk", [128, 64])
+def test_long_rows_column_slices(qk):
+    """Rows longer than one shared-memory stage are streamed in column slices."""
+    K = 65536 if qk == 128 else 32768   # 512 chunks per row: two column slices
+    N, B = 45, 1
+    blocks = synth.q1_0_blocks(N, K, seed=5) if qk == 128 else synth.q2_0_blocks(N, K, seed=5)
+    q, dx = _q8(B, K, seed=6)
+    _check_q(qk, blocks, q, dx)
+
+
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_grouped_trit(B):
+    K = 2560
+    Ns = [640, 640, 33, 1]
+    planes = [synth.trit_planes(n, K, seed=3000 + i)[0] for i, n in enumerate(Ns)]
+    q = synth.int8_codes(B, K, seed=3100)
+    xs = (np.abs(synth.activations(1, B, seed=3101)[0]) * 0.01 + 1e-3).astype(np.float32)
+    mats, outs = [], []
+    for i, (n, pl) in enumerate(zip(Ns, planes)):
+        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
+        acc = torch.empty((B, n), dtype=torch.int32, device="cuda") if i != 1 else None
+        mats.append((dev(pl), 0.01 * (i + 1), y, acc, n))
+        outs.append((y, acc, 0.01 * (i + 1)))
+    lb.lb_gemv_trit_planes_grouped(mats, dev(q), dev(xs), K, B)
+    torch.cuda.synchronize()
+    for pl, (y, acc, ws) in zip(planes, outs):
+        acc_ref, y_ref = oracle.trit_planes_product(pl, ws, q, xs)
+        assert np.array_equal(host(y).view(np.uint32), y_ref.view(np.uint32))
+        if acc is not None:
+            assert np.array_equal(host(acc), acc_ref)
+
+
+def test_device_status_clean():
+    assert lb.lb_device_status() == 0
