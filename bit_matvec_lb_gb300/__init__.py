@@ -26,9 +26,12 @@ LB_STATUS = {0: "LB_OK", -1: "LB_ERR_NULL", -2: "LB_ERR_ALIGN", -3: "LB_ERR_SHAP
 
 
 class LBError(RuntimeError):
-    def __init__(self, fn: str, status: int):
+    def __init__(self, fn: str, status: int, cuda_error: str = ""):
         self.status = status
-        super().__init__(f"{fn} returned {status} ({LB_STATUS.get(status, 'LB_ERR_UNKNOWN')})")
+        self.cuda_error = cuda_error
+        extra = f", {cuda_error}" if cuda_error else ""
+        super().__init__(
+            f"{fn} returned {status} ({LB_STATUS.get(status, 'LB_ERR_UNKNOWN')}{extra})")
 
 
 _lib = None
@@ -52,6 +55,8 @@ class lb_trit_matrix(ctypes.Structure):
 SIGNATURES = {
     "lb_status_string": (ctypes.c_char_p, [I32]),
     "lb_version": (I32, []),
+    "lb_last_cuda_error": (I32, []),
+    "lb_cuda_error_name": (ctypes.c_char_p, [I32]),
     "lb_quantize_q8_0": (I32, [P, P, P, I64, I64, P]),
     "lb_quantize_i8_absmax": (I32, [P, P, P, I64, I64, P]),
     "lb_repack_q1_0": (I32, [P, I64, I64, P, P, P]),
@@ -65,6 +70,9 @@ SIGNATURES = {
     "lb_gemv_q2_0_g64_grouped": (I32, [ctypes.POINTER(lb_q_matrix), I32, P, P, I64, I32, P]),
     "lb_gemv_trit_planes_grouped": (I32, [ctypes.POINTER(lb_trit_matrix), I32, P, P, I64, I32,
                                           P]),
+    "lb_gemm_workspace_bytes": (ctypes.c_size_t, [I64, I64]),
+    "lb_gemm_q1_0": (I32, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
+    "lb_gemm_q2_0_g64": (I32, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
 }
 
 
@@ -125,7 +133,21 @@ def _stream(stream):
 
 def _check(fn: str, status: int):
     if status != 0:
-        raise LBError(fn, status)
+        cuda = ""
+        if status == -6:  # LB_ERR_LAUNCH
+            code = load().lb_last_cuda_error()
+            if code:
+                cuda = load().lb_cuda_error_name(code).decode()
+        raise LBError(fn, status, cuda)
+
+
+def lb_last_cuda_error() -> int:
+    """cudaError_t of the library's last failed CUDA call on this thread (then reset), or 0."""
+    return int(load().lb_last_cuda_error())
+
+
+def lb_cuda_error_name(code: int) -> str:
+    return load().lb_cuda_error_name(int(code)).decode()
 
 
 def lb_quantize_q8_0(x, q, d, B: int, K: int, stream=None):
@@ -208,3 +230,29 @@ def lb_gemv_trit_planes_grouped(mats, q, x_scale, K: int, B: int, stream=None):
         arr[i] = lb_trit_matrix(_ptr(planes), float(w_scale), _ptr(y), _ptr(acc), int(N))
     _check("lb_gemv_trit_planes_grouped", load().lb_gemv_trit_planes_grouped(
         arr, len(mats), _ptr(q), _ptr(x_scale), K, B, _stream(stream)))
+
+
+def lb_gemm_workspace_bytes(M: int, K: int) -> int:
+    """Bytes of device scratch lb_gemm_* needs for M tokens of K columns."""
+    return int(load().lb_gemm_workspace_bytes(int(M), int(K)))
+
+
+def _gemm(name, bits, scales, q, d, y, M, N, K, workspace, workspace_bytes, stream):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    nbytes = int(workspace_bytes)
+    _check(name, getattr(load(), name)(_ptr(bits), _ptr(scales), _ptr(q), _ptr(d), _ptr(y),
+                                       int(M), int(N), int(K), _ptr(workspace), nbytes,
+                                       _stream(stream)))
+
+
+def lb_gemm_q1_0(bits, scales, q, d, y, M: int, N: int, K: int, workspace,
+                 workspace_bytes=None, stream=None):
+    """workspace: a device tensor (its size is passed) or a pointer with workspace_bytes."""
+    _gemm("lb_gemm_q1_0", bits, scales, q, d, y, M, N, K, workspace, workspace_bytes, stream)
+
+
+def lb_gemm_q2_0_g64(codes, scales, q, d, y, M: int, N: int, K: int, workspace,
+                     workspace_bytes=None, stream=None):
+    _gemm("lb_gemm_q2_0_g64", codes, scales, q, d, y, M, N, K, workspace, workspace_bytes,
+          stream)

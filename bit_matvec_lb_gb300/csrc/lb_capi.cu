@@ -12,6 +12,13 @@
 
 namespace lb {
 
+static thread_local int g_last_cuda_error = 0;
+
+void record_cuda_error(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    cudaGetLastError();
+}
+
 static constexpr int kMaxDevices = 64;
 static DeviceInfo g_info[kMaxDevices];
 static std::mutex g_info_mutex;
@@ -78,18 +85,25 @@ int prepare_kernel(const void *kernel, int threads, size_t smem, int *blocks_per
         int dev = 0, optin = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
-            cudaSuccess) {
-            cudaGetLastError();
+        // The dynamic limit plus the kernel's static shared memory may not exceed the opt-in
+        // maximum.
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - (int)fa.sharedSizeBytes);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
             return LB_ERR_LAUNCH;
         }
         p.attr_set = true;
     }
     if (p.smem != smem || p.threads != threads) {
         int bps = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel, threads, smem) !=
-            cudaSuccess) {
-            cudaGetLastError();
+        const cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kernel, threads, smem);
+        if (e != cudaSuccess) {
+            record_cuda_error(e);
             return LB_ERR_LAUNCH;
         }
         p.smem = smem;
@@ -101,6 +115,16 @@ int prepare_kernel(const void *kernel, int threads, size_t smem, int *blocks_per
 }
 
 }  // namespace lb
+
+LB_EXPORT int lb_last_cuda_error(void) {
+    const int e = lb::g_last_cuda_error;
+    lb::g_last_cuda_error = 0;
+    return e;
+}
+
+LB_EXPORT const char *lb_cuda_error_name(int code) {
+    return cudaGetErrorName(static_cast<cudaError_t>(code));
+}
 
 LB_EXPORT const char *lb_status_string(int status) {
     switch (status) {

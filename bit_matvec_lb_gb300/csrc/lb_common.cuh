@@ -35,6 +35,10 @@ int prepare_kernel(const void *kernel, int threads, size_t smem, int *blocks_per
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Remember a failed CUDA call's error for lb_last_cuda_error() (calling thread) and clear it
+// from the runtime's last-error slot.
+void record_cuda_error(cudaError_t e);
+
 // Launch `kernel` with programmatic stream serialization allowed (see pdl_wait()).
 template <typename... KArgs, typename... Args>
 inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -49,9 +53,10 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess
-               ? LB_OK
-               : LB_ERR_LAUNCH;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess) return LB_OK;
+    record_cuda_error(e);
+    return LB_ERR_LAUNCH;
 }
 
 inline int launch_status() {

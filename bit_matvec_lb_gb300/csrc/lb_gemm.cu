@@ -1,0 +1,442 @@
+// lb_gemm.cu -- prefill GEMM: Q1_0 / Q2_0_g64 weights x q8_0 activations of M tokens, on the
+// 5th-generation tensor cores.
+//
+// Arithmetic, for token m, weight row n, weight block b and its q8_0 blocks j
+// ("bankml: verified low-bit inference on commodity CPUs -- a technical report", III.2-III.3 for
+// Q1_0 and the 1x4 prefill tile that reuses one weight block across several activation
+// columns, III.5 for Q2_0_g64):
+//     y[m][n] = sum_j d_x[m][j] * (d_w[n][b(j)] * isum[m][n][j])
+// where isum is the integer dot product of the 32 weights of block j with the 32 int8 codes.
+//
+// GPU design: exact integers on the f16 tensor-core path (tcgen05.mma kind::f16; the int8 kind
+// does not exist on this architecture).
+//   * Activations: every q8_0 code is an integer in [-128, 127], exact in f16.  A prologue kernel
+//     converts q once into f16 tiles already laid out as the tensor core reads them from shared
+//     memory (K-major core matrices, lb_tc.cuh), so the main kernel moves them with one bulk
+//     copy per 128x32 tile.  The tiles live in a caller-provided workspace.
+//   * Weights: expanded in shared memory to W' = w * d_w (w in {-1, +1} or {-1, 0, +1, +2}),
+//     which is exact in f16.  The K order inside each 32-wide block is permuted (identically in
+//     the activation tiles) so that one f16x2 pair comes from one shift and one mask of a packed
+//     weight word.
+//   * One 128x128x32 step is two 16-deep MMAs into a tensor-memory accumulator: its value
+//     d_w * isum has at most 24 significant bits (|isum| <= 8192, d_w has 11), so it is exact in
+//     fp32.  Each 32-wide block is drained separately (d_x changes every 32 columns of K): the
+//     drain warps read the accumulator with tcgen05.ld and add d_x * (d_w * isum) with one FFMA
+//     per element into registers, flushing to y every 32 blocks, so the fp32 accumulation depth
+//     stays below 32 + K/1024.  Two accumulators alternate so MMAs overlap the drain.
+//   * Warp roles in a 512-thread CTA: warps 0-3 expand weights (one row each), warp 4 copies
+//     activation tiles, warp 5 owns tensor memory and issues the MMAs (one thread), warps 8-15
+//     (two warpgroups) drain.  A 4-stage shared-memory ring of {A tile, B tile} decouples them;
+//     every wait is bounded and reports through the device error word.
+#include "lb_tc.cuh"
+
+namespace lb {
+
+constexpr int kGemmThreads = 512;
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+constexpr int kGemmStages = 4;
+constexpr int kTileBytes = 8192;                 // 128 rows x 32 f16
+constexpr int kStageBytes = 2 * kTileBytes;      // A tile + B tile
+constexpr int kSeg = 32;                         // K32 blocks per drain segment
+constexpr int kWin = 8;                          // K32 blocks per expander prefetch window
+constexpr int kTotPitch = kTileM + 1;            // totals [n][m] pitch (conflict-free both ways)
+constexpr int kTotBytes = kTileN * kTotPitch * 4;
+constexpr int kGemmSmem = kGemmStages * kStageBytes + kTotBytes + 1024;
+
+enum GFmt { kG1 = 0, kG2 = 1 };
+
+struct GemmParams {
+    const uint8_t *bits;     // [N][K/8] (Q1_0) or [N][K/4] (Q2_0_g64)
+    const uint16_t *scales;  // [N][S]
+    const uint8_t *ws;       // activation tiles [mtiles][K/32][8192 B]
+    const uint16_t *d;       // [M][K/32] q8_0 scales
+    float *y;                // [M][N]
+    int *err;
+    int M, N, K, S, nK32, mtiles;
+};
+
+// ------------------------------------------------------------------------------------------
+// Prologue: q8_0 codes -> f16 activation tiles in the K-major core-matrix layout, with the
+// format's K permutation.  Chunk kc (8 positions) of a 32-wide block holds the byte
+// interleave of two source words:  Q2_0_g64 words (4(kc/2) + kc%2, +2), Q1_0 words (kc, kc+4).
+// Rows past M are zero.  One thread per (tile row, K32 block), rows fastest.
+// ------------------------------------------------------------------------------------------
+template <int F>
+__global__ void __launch_bounds__(256) gemm_prep_act_kernel(const int8_t *__restrict__ q,
+                                                            uint8_t *__restrict__ ws, int M,
+                                                            int K, int mtiles) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int nK32 = K / 32;
+    const int64_t total = (int64_t)mtiles * nK32 * kTileM;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int r = (int)(i % kTileM);
+        const int64_t tj = i / kTileM;
+        const int j = (int)(tj % nK32);
+        const int t = (int)(tj / nK32);
+        const int64_t row = (int64_t)t * kTileM + r;
+        uint32_t a[8];
+        if (row < M) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(q + row * K + (int64_t)j * 32);
+            const uint4 lo = src[0], hi = src[1];
+            a[0] = lo.x; a[1] = lo.y; a[2] = lo.z; a[3] = lo.w;
+            a[4] = hi.x; a[5] = hi.y; a[6] = hi.z; a[7] = hi.w;
+        } else {
+#pragma unroll
+            for (int w = 0; w < 8; w++) a[w] = 0;
+        }
+        uint8_t *tile = ws + ((int64_t)t * nK32 + j) * kTileBytes;
+#pragma unroll
+        for (int kc = 0; kc < 4; kc++) {
+            const uint32_t x = F == kG2 ? a[4 * (kc >> 1) + (kc & 1)] : a[kc];
+            const uint32_t y = F == kG2 ? a[4 * (kc >> 1) + (kc & 1) + 2] : a[kc + 4];
+            const uint32_t lo = prmt(x, y, 0x5140) ^ 0x80808080u;  // x0 y0 x1 y1, biased +128
+            const uint32_t hi = prmt(x, y, 0x7362) ^ 0x80808080u;  // x2 y2 x3 y3
+            // f16 with exponent byte 0x64: 1024 + (q + 128); subtracting 1152 (0x6480) gives q
+            uint32_t h[4] = {prmt(lo, 0x64646464u, 0x5140), prmt(lo, 0x64646464u, 0x7362),
+                             prmt(hi, 0x64646464u, 0x5140), prmt(hi, 0x64646464u, 0x7362)};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&h[e]), bias);
+                h[e] = *reinterpret_cast<uint32_t *>(&v);
+            }
+            *reinterpret_cast<uint4 *>(tile + canon_offset(r, kc * 8)) =
+                make_uint4(h[0], h[1], h[2], h[3]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Weight expansion of one 32-wide block of one row into its four 16-byte chunks.
+//   Q2_0_g64: code words w0 (codes 0..15) and w1 (16..31); f16x2 number s of word u holds codes
+//             (16u + s, 16u + s + 8): (w >> 2s) & 0x00030003 are the two codes in separate
+//             halves; (1024 + c) - 1025 = c - 1, times d_w.  f16x2 number i = 8u + s goes to
+//             chunk i / 4, slot i % 4.
+//   Q1_0:     sign word w; f16x2 number i (0..15) holds weights (i, i + 16): bits i and i + 16
+//             shifted to bits 15 and 31 select the sign of d_w.  Chunk i / 4, slot i % 4.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void expand_q2(uint32_t w0, uint32_t w1, __half d, uint4 (&c)[4]) {
+    const __half2 d2 = __halves2half2(d, d);
+    const __half2 k1025 = __halves2half2(__ushort_as_half(0x6401), __ushort_as_half(0x6401));
+    uint32_t o[16];
+#pragma unroll
+    for (int u = 0; u < 2; u++) {
+        const uint32_t w = u ? w1 : w0;
+#pragma unroll
+        for (int s = 0; s < 8; s++) {
+            uint32_t x = ((w >> (2 * s)) & 0x00030003u) | 0x64006400u;
+            __half2 v = __hmul2(__hsub2(*reinterpret_cast<__half2 *>(&x), k1025), d2);
+            o[8 * u + s] = *reinterpret_cast<uint32_t *>(&v);
+        }
+    }
+#pragma unroll
+    for (int kc = 0; kc < 4; kc++)
+        c[kc] = make_uint4(o[4 * kc], o[4 * kc + 1], o[4 * kc + 2], o[4 * kc + 3]);
+}
+
+__device__ __forceinline__ void expand_q1(uint32_t w, uint16_t dbits, uint4 (&c)[4]) {
+    const uint32_t dd = (uint32_t)dbits | ((uint32_t)dbits << 16);
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const uint32_t x = w << (15 - i);
+        o[i] = dd ^ (~x & 0x80008000u);  // set bit: +d_w, clear bit: -d_w
+    }
+#pragma unroll
+    for (int kc = 0; kc < 4; kc++)
+        c[kc] = make_uint4(o[4 * kc], o[4 * kc + 1], o[4 * kc + 2], o[4 * kc + 3]);
+}
+
+__device__ __forceinline__ bool wait_or_report(uint64_t *bar, uint32_t parity, int *err) {
+    if (mbar_wait(bar, parity)) return true;
+    if (err) atomicOr(err, 1);
+    return false;
+}
+
+template <int F>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t gsm_raw[];
+    uint8_t *gsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) &
+                                               ~(uintptr_t)1023);
+    __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages], tfull[2], tempty[2],
+        mma_done;
+    __shared__ uint32_t tmem_slot;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.x % p.mtiles;
+    const int n_tile = blockIdx.x / p.mtiles;
+    const int64_t m0 = (int64_t)m_tile * kTileM, n0 = (int64_t)n_tile * kTileN;
+    const int nK32 = p.nK32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGemmStages; s++) {
+            mbar_init(&full[s], 5);   // four expander warps + the activation copy
+            mbar_init(&empty[s], 1);  // MMA completion
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&tfull[b], 1);  // MMA completion
+            mbar_init(&tempty[b], 8); // eight drain warps
+        }
+        mbar_init(&mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(&tmem_slot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    pdl_launch_dependents();
+
+    if (warp < 4) {
+        // ---------------- weight expanders: one row each ----------------
+        const int nl = threadIdx.x;
+        const int64_t n = n0 + nl;
+        const bool valid = n < p.N;
+        const int rowbytes = F == kG2 ? p.K / 4 : p.K / 8;
+        const int nblk = F == kG2 ? p.K / 64 : p.K / 128;
+        const uint8_t *row = p.bits + (valid ? n : 0) * (int64_t)rowbytes;
+        const uint16_t *srow = p.scales + (valid ? n : 0) * (int64_t)p.S;
+        constexpr int kVec = F == kG2 ? 4 : 2;      // uint4 of codes per window
+        constexpr int kScl = F == kG2 ? 4 : 2;      // scales per window
+        const int nwin = (nK32 + kWin - 1) / kWin;
+        uint4 cur[kVec], nxt[kVec];
+        uint16_t csc[kScl], nsc[kScl];
+        auto load_window = [&](int w, uint4 (&cw)[kVec], uint16_t (&cs)[kScl]) {
+#pragma unroll
+            for (int v = 0; v < kVec; v++) {
+                const int blk0 = w * kWin + v * (kWin / kVec);
+                cw[v] = (valid && blk0 < nK32)
+                            ? *reinterpret_cast<const uint4 *>(row + (int64_t)blk0 * (F == kG2 ? 8 : 4))
+                            : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int v = 0; v < kScl; v++) {
+                const int jb = w * kScl + v;
+                cs[v] = (valid && jb < nblk) ? srow[jb] : (uint16_t)0;
+            }
+        };
+        load_window(0, cur, csc);
+        bool ok = true;
+        for (int w = 0; w < nwin && ok; w++) {
+            if (w + 1 < nwin) load_window(w + 1, nxt, nsc);
+#pragma unroll
+            for (int i = 0; i < kWin; i++) {
+                const int j = w * kWin + i;
+                if (j >= nK32) break;
+                const int s = j % kGemmStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], ((j / kGemmStages) & 1) ^ 1))) {
+                    if (lane == 0) atomicOr(p.err, 1);
+                    ok = false;
+                    break;
+                }
+                uint4 c[4];
+                if (F == kG2) {
+                    const uint4 &v = cur[i / 2];
+                    const uint32_t w0 = (i & 1) ? v.z : v.x, w1 = (i & 1) ? v.w : v.y;
+                    expand_q2(w0, w1, __ushort_as_half(csc[i / 2]), c);
+                } else {
+                    const uint4 &v = cur[i / 4];
+                    const uint32_t ww = (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
+                    expand_q1(ww, csc[i / 4], c);
+                }
+                uint8_t *btile = gsm + (size_t)s * kStageBytes + kTileBytes;
+#pragma unroll
+                for (int kc = 0; kc < 4; kc++)
+                    *reinterpret_cast<uint4 *>(btile + canon_offset(nl, kc * 8)) = c[kc];
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+            }
+#pragma unroll
+            for (int v = 0; v < kVec; v++) cur[v] = nxt[v];
+#pragma unroll
+            for (int v = 0; v < kScl; v++) csc[v] = nsc[v];
+        }
+    } else if (warp == 4) {
+        // ---------------- activation tiles: one bulk copy per step ----------------
+        pdl_wait();
+        if (lane == 0) {
+            const uint8_t *src = p.ws + (int64_t)m_tile * nK32 * kTileBytes;
+            int issued = 0;
+            for (int j = 0; j < nK32; j++) {
+                const int s = j % kGemmStages;
+                if (!wait_or_report(&empty[s], ((j / kGemmStages) & 1) ^ 1, p.err)) break;
+                mbar_arrive_expect_tx(&full[s], kTileBytes);
+                bulk_g2s(gsm + (size_t)s * kStageBytes, src + (int64_t)j * kTileBytes, kTileBytes,
+                         &full[s]);
+                issued = j + 1;
+            }
+            // No copy may still be landing in shared memory when the CTA exits: wait for the
+            // stages issued last (immediate on the normal path, bounded on an error path).
+            for (int j = max(0, issued - kGemmStages); j < issued; j++)
+                mbar_wait(&full[j % kGemmStages], (j / kGemmStages) & 1);
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(kTileM, kTileN);
+            for (int j = 0; j < nK32; j++) {
+                const int s = j % kGemmStages, b = j & 1;
+                if (!wait_or_report(&full[s], (j / kGemmStages) & 1, p.err)) break;
+                if (!wait_or_report(&tempty[b], ((j >> 1) & 1) ^ 1, p.err)) break;
+                tc_fence_after();
+                const uint32_t sa = smem_u32(gsm + (size_t)s * kStageBytes);
+                const uint64_t ad = smem_desc(sa), bd = smem_desc(sa + kTileBytes);
+                const uint32_t d = tmem + (uint32_t)(b * kTileN);
+                mma_f16(d, ad, bd, idesc, 0u);
+                mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);
+                mma_commit(&empty[s]);
+                mma_commit(&tfull[b]);
+            }
+            // Every MMA issued has completed before tensor memory is released.
+            mma_commit(&mma_done);
+            wait_or_report(&mma_done, 0, p.err);
+        }
+    } else if (warp >= 8) {
+        // ---------------- drain: d_x * (d_w * isum) into registers ----------------
+        // Thread = token row (lane quarter of its warp), 64 weight columns per warpgroup.  Each
+        // 32-block segment is added into per-CTA totals in shared memory (laid out [n][m] with
+        // pitch 129, conflict-free for this column-wise access and for the row-wise store).
+        pdl_wait();
+        float *tot = reinterpret_cast<float *>(gsm + kGemmStages * kStageBytes);
+        const int g = (warp - 8) >> 2, lq = warp & 3;
+        const int mrow = lq * 32 + lane;
+        const int64_t m = m0 + mrow;
+        const bool mvalid = m < p.M;
+        const int col0 = g * 64;
+        const uint16_t *drow = p.d + (mvalid ? m : 0) * (int64_t)nK32;
+        uint64_t acc[32];
+#pragma unroll
+        for (int c = 0; c < 32; c++) acc[c] = 0;
+        bool first = true;
+        float dx_next = mvalid ? f16_bits_to_float(drow[0]) : 0.0f;
+        for (int j = 0; j < nK32; j++) {
+            const int b = j & 1;
+            const uint32_t dxb = __float_as_uint(dx_next);
+            const uint64_t dx2 = ((uint64_t)dxb << 32) | dxb;
+            if (j + 1 < nK32) dx_next = mvalid ? f16_bits_to_float(drow[j + 1]) : 0.0f;
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], (j >> 1) & 1))) {
+                if (lane == 0) atomicOr(p.err, 1);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(b * kTileN + col0);
+            uint32_t r[32];
+            tmem_ld32(taddr, r);
+#pragma unroll
+            for (int c = 0; c < 16; c++) ffma2(acc[c], r[2 * c], r[2 * c + 1], dx2);
+            tmem_ld32(taddr + 32, r);
+#pragma unroll
+            for (int c = 0; c < 16; c++) ffma2(acc[16 + c], r[2 * c], r[2 * c + 1], dx2);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+            if ((j + 1) % kSeg == 0 || j + 1 == nK32) {
+                float *t = tot + col0 * kTotPitch + mrow;
+#pragma unroll
+                for (int c = 0; c < 32; c++) {
+                    const float lo = __uint_as_float((uint32_t)acc[c]);
+                    const float hi = __uint_as_float((uint32_t)(acc[c] >> 32));
+                    float *t0 = t + (2 * c) * kTotPitch, *t1 = t0 + kTotPitch;
+                    *t0 = first ? lo : *t0 + lo;
+                    *t1 = first ? hi : *t1 + hi;
+                    acc[c] = 0;
+                }
+                first = false;
+            }
+        }
+        // All eight drain warps are done with the totals: store the tile, one 128-byte row
+        // segment per warp instruction.
+        named_sync(1, 256);
+        const int wd = warp - 8;
+        for (int rr = 0; rr < kTileM / 8; rr++) {
+            const int ml = wd * (kTileM / 8) + rr;
+            const int64_t mm = m0 + ml;
+            if (mm >= p.M) break;
+            float *yrow = p.y + mm * (int64_t)p.N;
+#pragma unroll
+            for (int i = 0; i < kTileN / 32; i++) {
+                const int nl = i * 32 + lane;
+                if (n0 + nl < p.N) yrow[n0 + nl] = tot[nl * kTotPitch + ml];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+static int gemm_q(int F, const uint8_t *bits, const uint16_t *scales, const int8_t *q,
+                  const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+    const int qk = F == kG1 ? 128 : 64;
+    if (!bits || !scales || !q || !d || !y || !workspace) return LB_ERR_NULL;
+    if (!aligned16(bits) || !aligned16(scales) || !aligned16(q) || !aligned16(d) ||
+        !aligned16(y) || !aligned16(workspace))
+        return LB_ERR_ALIGN;
+    if (M < 1 || N < 1 || K < qk || K % qk != 0 || M > (1 << 30) || N > (1 << 30) ||
+        K > (1 << 24))
+        return LB_ERR_SHAPE;
+    const int64_t mtiles = (M + kTileM - 1) / kTileM;
+    const int64_t ntiles = (N + kTileN - 1) / kTileN;
+    if (workspace_bytes < (size_t)(mtiles * kTileM * K * 2)) return LB_ERR_SHAPE;
+    if (mtiles * ntiles > 0x7fffffff) return LB_ERR_SHAPE;
+    DeviceInfo di;
+    if (int st = current_device_info(&di)) return st;
+    cudaStream_t st = as_stream(stream);
+    // prologue: activation tiles
+    const int64_t work = mtiles * kTileM * (K / 32);
+    int64_t pgrid = (work + 255) / 256;
+    if (pgrid > (int64_t)di.sms * 16) pgrid = (int64_t)di.sms * 16;
+    int e = F == kG1 ? launch_pdl(gemm_prep_act_kernel<kG1>, dim3((unsigned)pgrid), dim3(256), 0,
+                                  st, q, (uint8_t *)workspace, (int)M, (int)K, (int)mtiles)
+                     : launch_pdl(gemm_prep_act_kernel<kG2>, dim3((unsigned)pgrid), dim3(256), 0,
+                                  st, q, (uint8_t *)workspace, (int)M, (int)K, (int)mtiles);
+    if (e) return e;
+    GemmParams p{};
+    p.bits = bits;
+    p.scales = scales;
+    p.ws = (const uint8_t *)workspace;
+    p.d = d;
+    p.y = y;
+    p.err = device_error_word();
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.S = (int)((K / qk + 7) / 8 * 8);
+    p.nK32 = (int)(K / 32);
+    p.mtiles = (int)mtiles;
+    auto kern = F == kG1 ? gemm_q_kernel<kG1> : gemm_q_kernel<kG2>;
+    int bps = 0;
+    if (int e2 = prepare_kernel(reinterpret_cast<const void *>(kern), kGemmThreads, kGemmSmem,
+                                &bps))
+        return e2;
+    return launch_pdl(kern, dim3((unsigned)(mtiles * ntiles)), dim3(kGemmThreads), kGemmSmem, st,
+                      p);
+}
+
+}  // namespace lb
+
+using namespace lb;
+
+LB_EXPORT size_t lb_gemm_workspace_bytes(int64_t M, int64_t K) {
+    if (M < 1 || K < 1) return 0;
+    return (size_t)((M + kTileM - 1) / kTileM) * kTileM * (size_t)K * 2;
+}
+
+LB_EXPORT int lb_gemm_q1_0(const uint8_t *bits, const uint16_t *scales, const int8_t *q,
+                           const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    return gemm_q(kG1, bits, scales, q, d, y, M, N, K, workspace, workspace_bytes, stream);
+}
+
+LB_EXPORT int lb_gemm_q2_0_g64(const uint8_t *codes, const uint16_t *scales, const int8_t *q,
+                               const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    return gemm_q(kG2, codes, scales, q, d, y, M, N, K, workspace, workspace_bytes, stream);
+}

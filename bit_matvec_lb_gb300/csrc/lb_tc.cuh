@@ -1,0 +1,99 @@
+// lb_tc.cuh -- 5th-generation tensor core (tcgen05) helpers: tensor-memory allocation, MMA
+// issue, commit, tensor-memory loads, and the shared-memory / instruction descriptors.
+//
+// Operand layout used throughout: K-major, no swizzle.  A [rows][32] f16 tile is stored as core
+// matrices of 8 rows x 16 bytes (8 f16 of K):
+//     byte offset(r, k) = (r / 8) * 512 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2
+// i.e. leading-dimension byte offset (between K-adjacent core matrices) 128 and stride byte
+// offset (between 8-row groups) 512; one 16-deep MMA step reads two K-adjacent core matrices,
+// the second step starts 256 bytes further.
+#pragma once
+#include "lb_common.cuh"
+
+namespace lb {
+
+constexpr int kCoreLBO = 128;
+constexpr int kCoreSBO = 512;
+
+__device__ __forceinline__ int canon_offset(int r, int k) {
+    return (r >> 3) * kCoreSBO + (k >> 3) * kCoreLBO + (r & 7) * 16 + (k & 7) * 2;
+}
+
+// Shared-memory matrix descriptor: start address, LBO, SBO (all >> 4), version 1, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((kCoreLBO >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((kCoreSBO >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B f16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// D[tmem] (+)= A[desc] * B[desc]^T, cta_group::1, kind::f16.
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+// 32 consecutive columns of the calling warp's 32 lanes (lane quarter = warp id % 4).  The load
+// and its completion wait are one asm statement, so no use of r can be scheduled before the
+// data has arrived.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// acc (two binary32 in one 64-bit register, element 0 in the low half) += {a0, a1} * {s, s},
+// each element rounded once as by fmaf.
+__device__ __forceinline__ void ffma2(uint64_t &acc, uint32_t a0, uint32_t a1, uint64_t s2) {
+    asm("{ .reg .b64 t; mov.b64 t, {%1, %2}; fma.rn.f32x2 %0, t, %3, %0; }"
+        : "+l"(acc)
+        : "r"(a0), "r"(a1), "l"(s2));
+}
+
+}  // namespace lb

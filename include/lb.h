@@ -52,11 +52,18 @@ extern "C" {
 #define LB_ERR_SHAPE (-3)   /* a size is out of range or not a multiple of the block */
 #define LB_ERR_BATCH (-4)   /* GEMV batch outside [1, 8] */
 #define LB_ERR_ARCH (-5)    /* the current device is not compute capability 10.3 */
-#define LB_ERR_LAUNCH (-6)  /* the CUDA launch failed (the CUDA error is left pending) */
+#define LB_ERR_LAUNCH (-6)  /* a CUDA launch or kernel setup call failed (lb_last_cuda_error) */
 #define LB_ERR_DEVICE (-7)  /* a kernel gave up on a bounded wait (see lb_device_status) */
 
 /* Name of a status code ("LB_OK", "LB_ERR_SHAPE", ...); never NULL. */
 const char *lb_status_string(int status);
+
+/* The cudaError_t value of the last CUDA call of this library that failed on the calling thread
+ * (the cause behind LB_ERR_LAUNCH), then reset to 0; 0 if none failed since the last read. */
+int lb_last_cuda_error(void);
+
+/* CUDA's name for a cudaError_t value ("cudaErrorInvalidValue", ...); never NULL. */
+const char *lb_cuda_error_name(int code);
 
 /* Library version as 10000*major + 100*minor + patch. */
 int lb_version(void);
@@ -190,6 +197,34 @@ int lb_gemv_trit_planes_grouped(const lb_trit_matrix *mats, int G, const int8_t 
  * Accuracy: |y - exact| <= 1e-5 * sum_k |w x| + 1e-6. K % 8 == 0; N >= 1; B in [1, 8]. */
 int lb_gemv_bf16(const uint16_t *w, const float *x, float *y, int64_t N, int64_t K, int B,
                  void *stream);
+
+/* ---- Prefill GEMM ([TR] III.3: one weight block reused across several activation columns,
+ * the prefill tile).  Same arithmetic and accuracy as the GEMVs above, for M tokens:
+ *   y[m][n] = sum_k d_w[n][k] * sum_j d_x[m][j] * isum_j
+ * computed on the tensor cores as exact per-32-column partial products d_w * isum_j (integers
+ * times an fp16 scale, exact in binary32), each scaled by d_x[m][j] with one fused multiply-add
+ * into a binary32 accumulator of at most 32 + K/1024 additions.
+ *   bits / codes, scales : as lb_gemv_q1_0 / lb_gemv_q2_0_g64 (repacked).
+ *   q, d      : q8_0 activations [M][K] int8 and [M][K/32] fp16.
+ *   y         : [M][N] fp32, overwritten.
+ *   workspace : device scratch of at least lb_gemm_workspace_bytes(M, K) bytes, owned by the
+ *               caller; it receives the activations converted to the tensor-core operand
+ *               layout, and must not be used by another call that may run at the same time.
+ * Limits: 1 <= M, N <= 2^30; K % QK == 0 (QK = 128 for Q1_0, 64 for Q2_0_g64), K <= 2^24.
+ * Q2_0_g64 weight scales must satisfy |d_w| <= 32752 (so that 2 * d_w is finite in fp16);
+ * fp16 scales of real weights are many orders of magnitude smaller.
+ * Errors: LB_ERR_NULL, LB_ERR_ALIGN, LB_ERR_SHAPE (shape limits, or a workspace too small),
+ * LB_ERR_ARCH, LB_ERR_LAUNCH; a bounded wait that gives up sets the device status
+ * (lb_device_status). */
+size_t lb_gemm_workspace_bytes(int64_t M, int64_t K);  /* 0 for M < 1 or K < 1 */
+
+int lb_gemm_q1_0(const uint8_t *bits, const uint16_t *scales, const int8_t *q, const uint16_t *d,
+                 float *y, int64_t M, int64_t N, int64_t K, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+int lb_gemm_q2_0_g64(const uint8_t *codes, const uint16_t *scales, const int8_t *q,
+                     const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

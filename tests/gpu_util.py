@@ -72,3 +72,19 @@ def within(y, y_exact, mag, rel=1e-5, abs_=1e-6):
     tol = rel * mag + abs_
     ok = err <= tol
     return bool(np.all(ok)), float(np.max(err / tol)) if err.size else 0.0
+
+
+def gemm_q(qk: int, blocks: np.ndarray, q: np.ndarray, dx: np.ndarray, workspace=None,
+           repacked=None):
+    """Run lb_gemm_q1_0 (qk=128) or lb_gemm_q2_0_g64 (qk=64) over M = q.shape[0] tokens."""
+    N = blocks.shape[0]
+    M, K = q.shape
+    bits, scales = repacked if repacked is not None else repack_on_gpu(blocks, K, qk)
+    if workspace is None:
+        workspace = torch.empty(lb.lb_gemm_workspace_bytes(M, K), dtype=torch.uint8,
+                                device="cuda")
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    fn = lb.lb_gemm_q1_0 if qk == 128 else lb.lb_gemm_q2_0_g64
+    fn(bits, scales, dev(q), dev(dx), y, M, N, K, workspace)
+    torch.cuda.synchronize()
+    return host(y)

@@ -55,6 +55,12 @@ def test_status_strings(lib):
     assert lib.lb_version() >= 100
 
 
+def test_cuda_error_query(lib):
+    assert lib.lb_last_cuda_error() == 0          # nothing failed on this thread
+    assert lib.lb_cuda_error_name(0).decode() == "cudaSuccess"
+    assert lb.lb_cuda_error_name(1) == "cudaErrorInvalidValue"
+
+
 # Host-side refusals: these return before any CUDA call, so they run without a GPU.
 A = 0x10000          # 16-byte aligned fake device address (never dereferenced)
 MIS = 0x10008        # misaligned
@@ -138,3 +144,35 @@ def test_grouped_refusals(lib):
 def test_scale_stride():
     assert lb.scale_stride(512, 128) == 8 and lb.scale_stride(4096, 64) == 64
     assert lb.scale_stride(4224, 128) == 40 and lb.scale_stride(320, 64) == 8
+
+
+# ---- prefill GEMM: host checks ----
+def test_gemm_workspace_bytes(lib):
+    assert lib.lb_gemm_workspace_bytes(0, 128) == 0
+    assert lib.lb_gemm_workspace_bytes(1, 0) == 0
+    # tokens are rounded up to tiles of 128; two bytes per converted code
+    assert lib.lb_gemm_workspace_bytes(1, 128) == 128 * 128 * 2
+    assert lib.lb_gemm_workspace_bytes(128, 4096) == 128 * 4096 * 2
+    assert lib.lb_gemm_workspace_bytes(129, 4096) == 256 * 4096 * 2
+    assert lb.lb_gemm_workspace_bytes(512, 12288) == 512 * 12288 * 2
+
+
+@pytest.mark.parametrize("fn,qk", [("lb_gemm_q1_0", 128), ("lb_gemm_q2_0_g64", 64)])
+def test_gemm_refusals(lib, fn, qk):
+    f = getattr(lib, fn)
+    ws = lib.lb_gemm_workspace_bytes(16, 4 * qk)
+    ok = (A, A, A, A, A, 16, 8, 4 * qk, A, ws, None)
+    for i in (0, 1, 2, 3, 4, 8):
+        args = list(ok)
+        args[i] = None
+        assert f(*args) == -1
+    for i in (0, 1, 2, 3, 4, 8):
+        args = list(ok)
+        args[i] = MIS
+        assert f(*args) == -2
+    bad_shapes = [(0, 8, 4 * qk), (16, 0, 4 * qk), (16, 8, qk // 2), (16, 8, 4 * qk + 32),
+                  (16, 8, 0), (2**31, 8, 4 * qk)]
+    for M, N, K in bad_shapes:
+        assert f(A, A, A, A, A, M, N, K, A, 2**40, None) == -3
+    # workspace one byte short
+    assert f(A, A, A, A, A, 16, 8, 4 * qk, A, ws - 1, None) == -3
