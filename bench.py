@@ -61,13 +61,15 @@ def q1_bytes(N, K):
     return N * (K // 128) * 18
 
 
-def peaks():
+def peaks(tensor: bool = False):
+    """HBM GB/s (or, with tensor=True, dense bf16 TFLOP/s burst) and whether it was measured."""
+    key, fallback = ("bf16_tflops", 1900.0) if tensor else ("hbm_gbs", 6800.0)
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return fallback, "fallback"
 
 
 # ---------------------------------------------------------------------------------------------
@@ -511,6 +513,36 @@ def rows_measure(lb, out):
             "ms_per_token": round(ms, 4), "bytes": tot,
             "head_GB/s": round(HN * HK * 2 / (ms_head * 1e-3) / 1e9, 1),
             "body_GB/s": round(body_bytes / ((ms - ms_head) * 1e-3) / 1e9, 1)}
+    # (4) Qwen3-8B-shaped prefill: 512 tokens through one layer's seven projections, Q1_0 and
+    #     Q2_0_g64 (q8_0 quantization of the three distinct activations + seven GEMMs per pass)
+    M = synth.PREFILL_M
+    tflops, _ = peaks(tensor=True)
+    xs = {k: torch.from_numpy(synth.activations(M, k, seed=10 + k)).cuda() for k in (4096, 12288)}
+    qs = {k: torch.empty((M, k), dtype=torch.int8, device="cuda") for k in (4096, 12288)}
+    ds = {k: torch.empty((M, k // 32), dtype=torch.int16, device="cuda") for k in (4096, 12288)}
+    ws = torch.empty(lb.lb_gemm_workspace_bytes(M, 12288), dtype=torch.uint8, device="cuda")
+    ops = 2 * M * sum(n * k for _, n, k in synth.QWEN3_8B_PROJ)
+    for fmt in ("q2_0_g64", "q1_0"):
+        make = make_q2_weights if fmt == "q2_0_g64" else make_q1_weights
+        gemm = lb.lb_gemm_q2_0_g64 if fmt == "q2_0_g64" else lb.lb_gemm_q1_0
+        proj = [(make(n, k, synth.proj_seed(90_000, 0, i)), n, k)
+                for i, (_, n, k) in enumerate(synth.QWEN3_8B_PROJ)]
+        ys = [torch.empty((M, n), dtype=torch.float32, device="cuda") for _, n, _ in proj]
+
+        def layer():
+            for i, ((wb, sc), n, k) in enumerate(proj):
+                if i in (0, 3, 4, 6):  # attention input, attention output, FFN input, FFN mid
+                    lb.lb_quantize_q8_0(xs[k], qs[k], ds[k], M, k, stream=stream)
+                gemm(wb, sc, qs[k], ds[k], ys[i], M, n, k, ws, stream=stream)
+        ms = time_graph(Graph(layer, stream), reps=20)
+        tops = ops / (ms * 1e-3) / 1e12
+        rows[f"qwen3_8b_prefill_m512_{fmt}"] = {
+            "TOPS": round(tops, 1), "pct_tensor_peak": round(100 * tops / tflops, 1),
+            "ms_per_layer": round(ms, 4), "int8_equivalent_ops": ops,
+            "peak": f"{tflops} TFLOP/s dense bf16/f16 tensor (measured cuBLAS), the rate of the "
+                    f"exact f16 tensor-core path the GEMM runs on"}
+        del proj, ys
+        torch.cuda.empty_cache()
     out["rows"] = rows
 
 

@@ -171,14 +171,34 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 // Bounded wait on the phase with the given parity: true once it completes, false after about
 // `limit_ns` (the caller then reports through the error word and stops instead of hanging).
+// The first test is inline; the timed loop is a separate function so that the common case (the
+// phase has already completed) costs one try_wait and a branch.
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` while the phase is
+// incomplete (it resumes as soon as the phase completes), so waiting warps do not take issue
+// slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __noinline__ static bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
+                                                   uint64_t limit_ns) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; i++) {
+        if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
+        if ((i & 15u) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; i++) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
-    }
+    return mbar_wait_slow(bar, parity, limit_ns);
 }
 // Bulk copy global -> this CTA's shared memory; completion is counted on `bar` (tx bytes).
 // dst, src and bytes must be multiples of 16.

@@ -35,14 +35,17 @@ namespace lb {
 constexpr int kGemmThreads = 512;
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
-constexpr int kGemmStages = 4;
+constexpr int kStages = 8;                       // {activation tile, weight tile} stages
+constexpr int kIssuers = 2;                      // MMA-issuing warps, alternating K32 steps
+constexpr int kAccBufs = 4;                      // tensor-memory accumulators (128 columns each)
 constexpr int kTileBytes = 8192;                 // 128 rows x 32 f16
-constexpr int kStageBytes = 2 * kTileBytes;      // A tile + B tile
 constexpr int kSeg = 32;                         // K32 blocks per drain segment
 constexpr int kWin = 8;                          // K32 blocks per expander prefetch window
 constexpr int kTotPitch = kTileM + 1;            // totals [n][m] pitch (conflict-free both ways)
 constexpr int kTotBytes = kTileN * kTotPitch * 4;
-constexpr int kGemmSmem = kGemmStages * kStageBytes + kTotBytes + 1024;
+constexpr int kStageBytes = 2 * kTileBytes;       // shared memory: stages {A, B}, then totals
+constexpr int kTotOffset = kStages * kStageBytes;
+constexpr int kGemmSmem = kTotOffset + kTotBytes + 1024;
 
 enum GFmt { kG1 = 0, kG2 = 1 };
 
@@ -156,13 +159,26 @@ __device__ __forceinline__ bool wait_or_report(uint64_t *bar, uint32_t parity, i
     return false;
 }
 
+// Index and phase parity of a ring of N stages (N a power of two), advanced one step at a time.
+template <int N>
+struct Ring {
+    int idx = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next() {
+        if (++idx == N) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 template <int F>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t gsm_raw[];
     uint8_t *gsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) &
                                                ~(uintptr_t)1023);
-    __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages], tfull[2], tempty[2],
-        mma_done;
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[kAccBufs],
+        tempty[kAccBufs], mma_done;
     __shared__ uint32_t tmem_slot;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x % p.mtiles;
@@ -171,18 +187,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
     const int nK32 = p.nK32;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kGemmStages; s++) {
-            mbar_init(&full[s], 5);   // four expander warps + the activation copy
-            mbar_init(&empty[s], 1);  // MMA completion
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(&full[s], 5);   // four expander warps + the activation copy (and its bytes)
+            mbar_init(&empty[s], 1);  // completion of the MMAs that read the stage
         }
-        for (int b = 0; b < 2; b++) {
-            mbar_init(&tfull[b], 1);  // MMA completion
-            mbar_init(&tempty[b], 8); // eight drain warps
+        for (int b = 0; b < kAccBufs; b++) {
+            mbar_init(&tfull[b], 1);   // MMA completion
+            mbar_init(&tempty[b], 8);  // eight drain warps
         }
-        mbar_init(&mma_done, 1);
+        mbar_init(&mma_done, kIssuers);
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(&tmem_slot, 256);
+    if (warp == 5) tmem_alloc(&tmem_slot, kAccBufs * kTileN);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -190,43 +206,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
     pdl_launch_dependents();
 
     if (warp < 4) {
-        // ---------------- weight expanders: one row each ----------------
+        // ---------------- weight expanders: thread = weight row ----------------
+        // Packed weights are read straight from global memory one window (8 K32 blocks) ahead.
         const int nl = threadIdx.x;
         const int64_t n = n0 + nl;
         const bool valid = n < p.N;
-        const int rowbytes = F == kG2 ? p.K / 4 : p.K / 8;
-        const int nblk = F == kG2 ? p.K / 64 : p.K / 128;
-        const uint8_t *row = p.bits + (valid ? n : 0) * (int64_t)rowbytes;
-        const uint16_t *srow = p.scales + (valid ? n : 0) * (int64_t)p.S;
-        constexpr int kVec = F == kG2 ? 4 : 2;      // uint4 of codes per window
-        constexpr int kScl = F == kG2 ? 4 : 2;      // scales per window
+        const int64_t nn = valid ? n : 0;
+        constexpr int kBlkBytes = F == kG2 ? 8 : 4;       // packed bytes per K32 block and row
+        constexpr int kVec = kWin * kBlkBytes / 16;        // uint4 per window
+        const uint8_t *row = p.bits + nn * (int64_t)nK32 * kBlkBytes;
+        const uint16_t *srow = p.scales + nn * (int64_t)p.S;
         const int nwin = (nK32 + kWin - 1) / kWin;
-        uint4 cur[kVec], nxt[kVec];
-        uint16_t csc[kScl], nsc[kScl];
-        auto load_window = [&](int w, uint4 (&cw)[kVec], uint16_t (&cs)[kScl]) {
+        auto load_window = [&](int w, uint4 (&cw)[kVec], uint2 &sc) {
+            const int j = w * kWin;
 #pragma unroll
             for (int v = 0; v < kVec; v++) {
-                const int blk0 = w * kWin + v * (kWin / kVec);
-                cw[v] = (valid && blk0 < nK32)
-                            ? *reinterpret_cast<const uint4 *>(row + (int64_t)blk0 * (F == kG2 ? 8 : 4))
+                const int jv = j + v * (16 / kBlkBytes);
+                cw[v] = (valid && jv < nK32)
+                            ? *reinterpret_cast<const uint4 *>(row + (int64_t)jv * kBlkBytes)
                             : make_uint4(0, 0, 0, 0);
             }
-#pragma unroll
-            for (int v = 0; v < kScl; v++) {
-                const int jb = w * kScl + v;
-                cs[v] = (valid && jb < nblk) ? srow[jb] : (uint16_t)0;
-            }
+            // Scales of the window's weight blocks (4 for Q2_0_g64, 2 for Q1_0); the scale rows
+            // are padded with zeros to a multiple of 8 entries, so these loads stay in the row.
+            if (F == kG2)
+                sc = (valid && j < nK32) ? *reinterpret_cast<const uint2 *>(srow + j / 2)
+                                         : make_uint2(0, 0);
+            else
+                sc = make_uint2((valid && j < nK32)
+                                    ? *reinterpret_cast<const uint32_t *>(srow + j / 4) : 0u,
+                                0u);
         };
-        load_window(0, cur, csc);
+        uint4 cur[kVec], nxt[kVec];
+        uint2 cs, ns = make_uint2(0, 0);
+        load_window(0, cur, cs);
+        const uint32_t boff = (uint32_t)canon_offset(nl, 0) + kTileBytes;
+        Ring<kStages> rs;
         bool ok = true;
         for (int w = 0; w < nwin && ok; w++) {
-            if (w + 1 < nwin) load_window(w + 1, nxt, nsc);
+            if (w + 1 < nwin) load_window(w + 1, nxt, ns);
 #pragma unroll
             for (int i = 0; i < kWin; i++) {
-                const int j = w * kWin + i;
-                if (j >= nK32) break;
-                const int s = j % kGemmStages;
-                if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], ((j / kGemmStages) & 1) ^ 1))) {
+                if (w * kWin + i >= nK32) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase ^ 1u))) {
                     if (lane == 0) atomicOr(p.err, 1);
                     ok = false;
                     break;
@@ -234,55 +255,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
                 uint4 c[4];
                 if (F == kG2) {
                     const uint4 &v = cur[i / 2];
-                    const uint32_t w0 = (i & 1) ? v.z : v.x, w1 = (i & 1) ? v.w : v.y;
-                    expand_q2(w0, w1, __ushort_as_half(csc[i / 2]), c);
+                    const uint32_t sw = (i / 4) ? cs.y : cs.x;
+                    const uint16_t sb = (uint16_t)(((i / 2) & 1) ? (sw >> 16) : (sw & 0xFFFFu));
+                    expand_q2((i & 1) ? v.z : v.x, (i & 1) ? v.w : v.y, __ushort_as_half(sb), c);
                 } else {
                     const uint4 &v = cur[i / 4];
                     const uint32_t ww = (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
-                    expand_q1(ww, csc[i / 4], c);
+                    expand_q1(ww, (uint16_t)((i / 4) ? (cs.x >> 16) : (cs.x & 0xFFFFu)), c);
                 }
-                uint8_t *btile = gsm + (size_t)s * kStageBytes + kTileBytes;
+                uint8_t *bt = gsm + rs.idx * kStageBytes + boff;
 #pragma unroll
                 for (int kc = 0; kc < 4; kc++)
-                    *reinterpret_cast<uint4 *>(btile + canon_offset(nl, kc * 8)) = c[kc];
+                    *reinterpret_cast<uint4 *>(bt + kc * kCoreLBO) = c[kc];
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full[s]);
+                if (lane == 0) mbar_arrive(&full[rs.idx]);
+                rs.next();
             }
 #pragma unroll
             for (int v = 0; v < kVec; v++) cur[v] = nxt[v];
-#pragma unroll
-            for (int v = 0; v < kScl; v++) csc[v] = nsc[v];
+            cs = ns;
         }
     } else if (warp == 4) {
         // ---------------- activation tiles: one bulk copy per step ----------------
         pdl_wait();
         if (lane == 0) {
             const uint8_t *src = p.ws + (int64_t)m_tile * nK32 * kTileBytes;
+            Ring<kStages> rs;
             int issued = 0;
             for (int j = 0; j < nK32; j++) {
-                const int s = j % kGemmStages;
-                if (!wait_or_report(&empty[s], ((j / kGemmStages) & 1) ^ 1, p.err)) break;
-                mbar_arrive_expect_tx(&full[s], kTileBytes);
-                bulk_g2s(gsm + (size_t)s * kStageBytes, src + (int64_t)j * kTileBytes, kTileBytes,
-                         &full[s]);
+                if (!wait_or_report(&empty[rs.idx], rs.phase ^ 1u, p.err)) break;
+                mbar_arrive_expect_tx(&full[rs.idx], kTileBytes);
+                bulk_g2s(gsm + rs.idx * kStageBytes, src + (int64_t)j * kTileBytes, kTileBytes,
+                         &full[rs.idx]);
+                rs.next();
                 issued = j + 1;
             }
             // No copy may still be landing in shared memory when the CTA exits: wait for the
             // stages issued last (immediate on the normal path, bounded on an error path).
-            for (int j = max(0, issued - kGemmStages); j < issued; j++)
-                mbar_wait(&full[j % kGemmStages], (j / kGemmStages) & 1);
+            for (int j = max(0, issued - kStages); j < issued; j++)
+                mbar_wait(&full[j % kStages], (j / kStages) & 1);
         }
-    } else if (warp == 5) {
-        // ---------------- MMA issue (one thread) ----------------
+    } else if (warp >= 5 && warp < 5 + kIssuers) {
+        // ---------------- MMA issue: warp 5 + i issues the steps j = i (mod kIssuers) ----------
+        // Several issuers share the per-step cost of barrier waits, MMA issue and commits;
+        // their MMAs touch disjoint stages and accumulators.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(kTileM, kTileN);
-            for (int j = 0; j < nK32; j++) {
-                const int s = j % kGemmStages, b = j & 1;
-                if (!wait_or_report(&full[s], (j / kGemmStages) & 1, p.err)) break;
-                if (!wait_or_report(&tempty[b], ((j >> 1) & 1) ^ 1, p.err)) break;
+            const uint32_t sbase = smem_u32(gsm);
+            for (int j = warp - 5; j < nK32; j += kIssuers) {
+                const int s = j & (kStages - 1), b = j & (kAccBufs - 1);
+                if (!wait_or_report(&full[s], (uint32_t)(j / kStages) & 1u, p.err)) break;
+                if (!wait_or_report(&tempty[b], ((uint32_t)(j / kAccBufs) & 1u) ^ 1u, p.err)) break;
                 tc_fence_after();
-                const uint32_t sa = smem_u32(gsm + (size_t)s * kStageBytes);
+                const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
                 const uint64_t ad = smem_desc(sa), bd = smem_desc(sa + kTileBytes);
                 const uint32_t d = tmem + (uint32_t)(b * kTileN);
                 mma_f16(d, ad, bd, idesc, 0u);
@@ -296,55 +322,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
         }
     } else if (warp >= 8) {
         // ---------------- drain: d_x * (d_w * isum) into registers ----------------
-        // Thread = token row (lane quarter of its warp), 64 weight columns per warpgroup.  Each
-        // 32-block segment is added into per-CTA totals in shared memory (laid out [n][m] with
-        // pitch 129, conflict-free for this column-wise access and for the row-wise store).
+        // Thread = token row (the lane quarter of its warp), 64 weight columns per warpgroup.
+        // Each 32-block segment is added into per-CTA totals in shared memory, laid out [n][m]
+        // with pitch 129 (conflict-free for this column-wise access and for the row-wise store).
         pdl_wait();
-        float *tot = reinterpret_cast<float *>(gsm + kGemmStages * kStageBytes);
+        float *tot = reinterpret_cast<float *>(gsm + kTotOffset);
         const int g = (warp - 8) >> 2, lq = warp & 3;
         const int mrow = lq * 32 + lane;
         const int64_t m = m0 + mrow;
         const bool mvalid = m < p.M;
         const int col0 = g * 64;
         const uint16_t *drow = p.d + (mvalid ? m : 0) * (int64_t)nK32;
+        const bool dvec = (nK32 & 7) == 0;  // rows of d are 16-byte aligned
+        // The activation scales of 8 consecutive steps, loaded one group ahead.
+        auto load_dx8 = [&](int j) -> uint4 {
+            if (!mvalid || j >= nK32) return make_uint4(0, 0, 0, 0);
+            if (dvec) return *reinterpret_cast<const uint4 *>(drow + j);
+            uint32_t v[4];
+#pragma unroll
+            for (int t = 0; t < 4; t++)
+                v[t] = (j + 2 * t < nK32) ? *reinterpret_cast<const uint32_t *>(drow + j + 2 * t)
+                                          : 0u;
+            return make_uint4(v[0], v[1], v[2], v[3]);
+        };
         uint64_t acc[32];
 #pragma unroll
         for (int c = 0; c < 32; c++) acc[c] = 0;
-        bool first = true;
-        float dx_next = mvalid ? f16_bits_to_float(drow[0]) : 0.0f;
-        for (int j = 0; j < nK32; j++) {
-            const int b = j & 1;
-            const uint32_t dxb = __float_as_uint(dx_next);
-            const uint64_t dx2 = ((uint64_t)dxb << 32) | dxb;
-            if (j + 1 < nK32) dx_next = mvalid ? f16_bits_to_float(drow[j + 1]) : 0.0f;
-            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], (j >> 1) & 1))) {
-                if (lane == 0) atomicOr(p.err, 1);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(b * kTileN + col0);
-            uint32_t r[32];
-            tmem_ld32(taddr, r);
+        bool first = true, ok = true;
+        const uint32_t tlane = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)col0;
+        uint4 dq = load_dx8(0);
+        for (int j8 = 0; j8 < nK32 && ok; j8 += 8) {
+            const uint4 dcur = dq;
+            dq = load_dx8(j8 + 8);
 #pragma unroll
-            for (int c = 0; c < 16; c++) ffma2(acc[c], r[2 * c], r[2 * c + 1], dx2);
-            tmem_ld32(taddr + 32, r);
-#pragma unroll
-            for (int c = 0; c < 16; c++) ffma2(acc[16 + c], r[2 * c], r[2 * c + 1], dx2);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
-            if ((j + 1) % kSeg == 0 || j + 1 == nK32) {
-                float *t = tot + col0 * kTotPitch + mrow;
-#pragma unroll
-                for (int c = 0; c < 32; c++) {
-                    const float lo = __uint_as_float((uint32_t)acc[c]);
-                    const float hi = __uint_as_float((uint32_t)(acc[c] >> 32));
-                    float *t0 = t + (2 * c) * kTotPitch, *t1 = t0 + kTotPitch;
-                    *t0 = first ? lo : *t0 + lo;
-                    *t1 = first ? hi : *t1 + hi;
-                    acc[c] = 0;
+            for (int i = 0; i < 8; i++) {
+                const int j = j8 + i;
+                if (j >= nK32) break;
+                const int b = j & (kAccBufs - 1);
+                const uint32_t dw = i < 2 ? dcur.x : i < 4 ? dcur.y : i < 6 ? dcur.z : dcur.w;
+                const uint32_t dxb =
+                    __float_as_uint(f16_bits_to_float((uint16_t)((i & 1) ? (dw >> 16) : dw)));
+                const uint64_t dx2 = ((uint64_t)dxb << 32) | dxb;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&tfull[b], (uint32_t)(j / kAccBufs) & 1u))) {
+                    if (lane == 0) atomicOr(p.err, 1);
+                    ok = false;
+                    break;
                 }
-                first = false;
+                tc_fence_after();
+                const uint32_t taddr = tlane + (uint32_t)(b * kTileN);
+                uint64_t r[16];
+                tmem_ld32_pairs(taddr, r);
+#pragma unroll
+                for (int c = 0; c < 16; c++) ffma2p(acc[c], r[c], dx2);
+                tmem_ld32_pairs(taddr + 32, r);
+                // The accumulator is free once both halves are in registers.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);
+#pragma unroll
+                for (int c = 0; c < 16; c++) ffma2p(acc[16 + c], r[c], dx2);
+                if ((j + 1) % kSeg == 0 || j + 1 == nK32) {
+                    float *t = tot + col0 * kTotPitch + mrow;
+#pragma unroll
+                    for (int c = 0; c < 32; c++) {
+                        const float lo = __uint_as_float((uint32_t)acc[c]);
+                        const float hi = __uint_as_float((uint32_t)(acc[c] >> 32));
+                        float *t0 = t + (2 * c) * kTotPitch, *t1 = t0 + kTotPitch;
+                        *t0 = first ? lo : *t0 + lo;
+                        *t1 = first ? hi : *t1 + hi;
+                        acc[c] = 0;
+                    }
+                    first = false;
+                }
             }
         }
         // All eight drain warps are done with the totals: store the tile, one 128-byte row
@@ -367,7 +417,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
     __syncthreads();
     if (warp == 5) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, kAccBufs * kTileN);
     }
 }
 

@@ -88,6 +88,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// The same load, returned as 16 pairs of columns (2c, 2c + 1) in 64-bit registers (column 2c in
+// the low half), ready for paired f32x2 arithmetic without register moves.
+__device__ __forceinline__ void tmem_ld32_pairs(uint32_t taddr, uint64_t (&p)[16]) {
+    asm volatile(
+        "{ .reg .b32 r<32>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {r0,r1,r2,r3,r4,r5,r6,r7,r8,r9,r10,r11,r12,r13,"
+        "r14,r15,r16,r17,r18,r19,r20,r21,r22,r23,r24,r25,r26,r27,r28,r29,r30,r31}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {r0, r1}; mov.b64 %1, {r2, r3}; mov.b64 %2, {r4, r5};\n\t"
+        "mov.b64 %3, {r6, r7}; mov.b64 %4, {r8, r9}; mov.b64 %5, {r10, r11};\n\t"
+        "mov.b64 %6, {r12, r13}; mov.b64 %7, {r14, r15}; mov.b64 %8, {r16, r17};\n\t"
+        "mov.b64 %9, {r18, r19}; mov.b64 %10, {r20, r21}; mov.b64 %11, {r22, r23};\n\t"
+        "mov.b64 %12, {r24, r25}; mov.b64 %13, {r26, r27}; mov.b64 %14, {r28, r29};\n\t"
+        "mov.b64 %15, {r30, r31}; }"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]),
+          "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]),
+          "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// acc += a * {s, s} on pairs of binary32 (element 0 in the low half), each element rounded once
+// as by fmaf.
+__device__ __forceinline__ void ffma2p(uint64_t &acc, uint64_t a, uint64_t s2) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(s2));
+}
+
 // acc (two binary32 in one 64-bit register, element 0 in the low half) += {a0, a1} * {s, s},
 // each element rounded once as by fmaf.
 __device__ __forceinline__ void ffma2(uint64_t &acc, uint32_t a0, uint32_t a1, uint64_t s2) {
