@@ -73,7 +73,10 @@ SIGNATURES = {
     "lb_gemm_workspace_bytes": (ctypes.c_size_t, [I64, I64]),
     "lb_gemm_q1_0": (I32, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
     "lb_gemm_q2_0_g64": (I32, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
+    "lb_gemm_q2_0_g64_noalloc": (I32, [P, P, P, P, P, I64, I64, I64, P]),
 }
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def library_path() -> str:
@@ -256,3 +259,10 @@ def lb_gemm_q2_0_g64(codes, scales, q, d, y, M: int, N: int, K: int, workspace,
                      workspace_bytes=None, stream=None):
     _gemm("lb_gemm_q2_0_g64", codes, scales, q, d, y, M, N, K, workspace, workspace_bytes,
           stream)
+
+
+def lb_gemm_q2_0_g64_noalloc(codes, scales, q, d, y, M: int, N: int, K: int, stream=None):
+    """lb_gemm_q2_0_g64 with the library's fixed scratch (no workspace argument)."""
+    _check("lb_gemm_q2_0_g64_noalloc", load().lb_gemm_q2_0_g64_noalloc(
+        _ptr(codes), _ptr(scales), _ptr(q), _ptr(d), _ptr(y), int(M), int(N), int(K),
+        _stream(stream)))

@@ -490,3 +490,14 @@ LB_EXPORT int lb_gemm_q2_0_g64(const uint8_t *codes, const uint16_t *scales, con
                                void *workspace, size_t workspace_bytes, void *stream) {
     return gemm_q(kG2, codes, scales, q, d, y, M, N, K, workspace, workspace_bytes, stream);
 }
+
+namespace lb {
+// Entry for other translation units that bring their own scratch (same checks and launches as
+// lb_gemm_q1_0 / lb_gemm_q2_0_g64).
+int gemm_q_with_workspace(int q2, const uint8_t *bits, const uint16_t *scales, const int8_t *q,
+                          const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    return gemm_q(q2 ? kG2 : kG1, bits, scales, q, d, y, M, N, K, workspace, workspace_bytes,
+                  stream);
+}
+}  // namespace lb

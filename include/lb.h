@@ -226,6 +226,24 @@ int lb_gemm_q2_0_g64(const uint8_t *codes, const uint16_t *scales, const int8_t 
                      const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- Q2_0_g64 prefill GEMM without caller scratch.
+ * No counterpart in the source pages: a convenience of this library for callers that cannot
+ * allocate device memory.  Same arithmetic, accuracy, layouts and errors as lb_gemm_q2_0_g64,
+ * but the converted activations go to a fixed scratch array of LB_NOALLOC_SCRATCH_BYTES inside
+ * the library (a file-scope device array; the call itself allocates nothing).
+ *   Limit: round_up(M, 128) * K * 2 <= LB_NOALLOC_SCRATCH_BYTES (8 MiB), e.g. M = 512 with
+ *   K <= 8192, or M <= 256 with K = 12288; larger sizes are refused with LB_ERR_SHAPE before any
+ *   device work.  Nothing in the scratch needs to start at zero.
+ *   There is one scratch per device: calls that may run at the same time on one device (another
+ *   stream, another host thread) race on it and give wrong results; serialize them.
+ *   The first call on each device looks the scratch up (cudaGetSymbolAddress); make that first
+ *   call before capturing a stream into a CUDA graph. */
+#define LB_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+int lb_gemm_q2_0_g64_noalloc(const uint8_t *codes, const uint16_t *scales, const int8_t *q,
+                             const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K,
+                             void *stream);
+
 #ifdef __cplusplus
 }
 #endif
