@@ -35,15 +35,15 @@ namespace lb {
 constexpr int kGemmThreads = 512;
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
-constexpr int kStages = 8;                       // {activation tile, weight tile} stages
-constexpr int kIssuers = 2;                      // MMA-issuing warps, alternating K32 steps
+constexpr int kTileBytes = 8192;                 // one 128 x 32 f16 operand tile
+constexpr int kStages = 4;                       // stages of two K32 steps: {A, A, B, B}
+constexpr int kStageBytes = 4 * kTileBytes;
+constexpr int kIssuers = 2;                      // MMA-issuing warps, alternating stages
 constexpr int kAccBufs = 4;                      // tensor-memory accumulators (128 columns each)
-constexpr int kTileBytes = 8192;                 // 128 rows x 32 f16
 constexpr int kSeg = 32;                         // K32 blocks per drain segment
 constexpr int kWin = 8;                          // K32 blocks per expander prefetch window
 constexpr int kTotPitch = kTileM + 1;            // totals [n][m] pitch (conflict-free both ways)
 constexpr int kTotBytes = kTileN * kTotPitch * 4;
-constexpr int kStageBytes = 2 * kTileBytes;       // shared memory: stages {A, B}, then totals
 constexpr int kTotOffset = kStages * kStageBytes;
 constexpr int kGemmSmem = kTotOffset + kTotBytes + 1024;
 
@@ -177,24 +177,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
     extern __shared__ uint8_t gsm_raw[];
     uint8_t *gsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) &
                                                ~(uintptr_t)1023);
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[kAccBufs],
-        tempty[kAccBufs], mma_done;
+    // full[s]: the stage's two A tiles have landed and its two B tiles are written.
+    // empty[s]: the stage's four MMAs have completed -- the stage may be refilled, and the two
+    //           accumulators it wrote may be drained.
+    // tempty[b]: accumulator b has been read out by the eight drain warps.
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tempty[kAccBufs], mma_done;
     __shared__ uint32_t tmem_slot;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x % p.mtiles;
     const int n_tile = blockIdx.x / p.mtiles;
     const int64_t m0 = (int64_t)m_tile * kTileM, n0 = (int64_t)n_tile * kTileN;
-    const int nK32 = p.nK32;
+    const int nK32 = p.nK32;       // even: K is a multiple of 64
+    const int nst = nK32 / 2;      // stages of two K32 steps
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(&full[s], 5);   // four expander warps + the activation copy (and its bytes)
-            mbar_init(&empty[s], 1);  // completion of the MMAs that read the stage
+            mbar_init(&empty[s], 1);  // commit after the stage's MMAs
         }
-        for (int b = 0; b < kAccBufs; b++) {
-            mbar_init(&tfull[b], 1);   // MMA completion
-            mbar_init(&tempty[b], 8);  // eight drain warps
-        }
+        for (int b = 0; b < kAccBufs; b++) mbar_init(&tempty[b], 8);  // eight drain warps
         mbar_init(&mma_done, kIssuers);
         fence_mbar_init();
     }
@@ -239,34 +240,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
         uint4 cur[kVec], nxt[kVec];
         uint2 cs, ns = make_uint2(0, 0);
         load_window(0, cur, cs);
-        const uint32_t boff = (uint32_t)canon_offset(nl, 0) + kTileBytes;
+        const uint32_t boff = (uint32_t)canon_offset(nl, 0) + 2 * kTileBytes;
         Ring<kStages> rs;
         bool ok = true;
         for (int w = 0; w < nwin && ok; w++) {
             if (w + 1 < nwin) load_window(w + 1, nxt, ns);
 #pragma unroll
-            for (int i = 0; i < kWin; i++) {
-                if (w * kWin + i >= nK32) break;
+            for (int h = 0; h < kWin / 2; h++) {  // one stage = K32 blocks 2h, 2h + 1 of the window
+                if (w * kWin + 2 * h >= nK32) break;
                 if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase ^ 1u))) {
                     if (lane == 0) atomicOr(p.err, 1);
                     ok = false;
                     break;
                 }
-                uint4 c[4];
-                if (F == kG2) {
-                    const uint4 &v = cur[i / 2];
-                    const uint32_t sw = (i / 4) ? cs.y : cs.x;
-                    const uint16_t sb = (uint16_t)(((i / 2) & 1) ? (sw >> 16) : (sw & 0xFFFFu));
-                    expand_q2((i & 1) ? v.z : v.x, (i & 1) ? v.w : v.y, __ushort_as_half(sb), c);
-                } else {
-                    const uint4 &v = cur[i / 4];
-                    const uint32_t ww = (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
-                    expand_q1(ww, (uint16_t)((i / 4) ? (cs.x >> 16) : (cs.x & 0xFFFFu)), c);
-                }
                 uint8_t *bt = gsm + rs.idx * kStageBytes + boff;
 #pragma unroll
-                for (int kc = 0; kc < 4; kc++)
-                    *reinterpret_cast<uint4 *>(bt + kc * kCoreLBO) = c[kc];
+                for (int t = 0; t < 2; t++) {
+                    const int i = 2 * h + t;
+                    uint4 c[4];
+                    if (F == kG2) {
+                        const uint4 &v = cur[i / 2];
+                        const uint32_t sw = (i / 4) ? cs.y : cs.x;
+                        const uint16_t sb = (uint16_t)(((i / 2) & 1) ? (sw >> 16) : (sw & 0xFFFFu));
+                        expand_q2((i & 1) ? v.z : v.x, (i & 1) ? v.w : v.y, __ushort_as_half(sb), c);
+                    } else {
+                        const uint4 &v = cur[i / 4];
+                        const uint32_t ww =
+                            (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
+                        expand_q1(ww, (uint16_t)((i / 4) ? (cs.x >> 16) : (cs.x & 0xFFFFu)), c);
+                    }
+#pragma unroll
+                    for (int kc = 0; kc < 4; kc++)
+                        *reinterpret_cast<uint4 *>(bt + t * kTileBytes + kc * kCoreLBO) = c[kc];
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[rs.idx]);
@@ -277,44 +283,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
             cs = ns;
         }
     } else if (warp == 4) {
-        // ---------------- activation tiles: one bulk copy per step ----------------
+        // ---------------- activation tiles: one 16 KB bulk copy per stage ----------------
         pdl_wait();
         if (lane == 0) {
             const uint8_t *src = p.ws + (int64_t)m_tile * nK32 * kTileBytes;
             Ring<kStages> rs;
             int issued = 0;
-            for (int j = 0; j < nK32; j++) {
+            for (int st = 0; st < nst; st++) {
                 if (!wait_or_report(&empty[rs.idx], rs.phase ^ 1u, p.err)) break;
-                mbar_arrive_expect_tx(&full[rs.idx], kTileBytes);
-                bulk_g2s(gsm + rs.idx * kStageBytes, src + (int64_t)j * kTileBytes, kTileBytes,
-                         &full[rs.idx]);
+                mbar_arrive_expect_tx(&full[rs.idx], 2 * kTileBytes);
+                bulk_g2s(gsm + rs.idx * kStageBytes, src + (int64_t)st * 2 * kTileBytes,
+                         2 * kTileBytes, &full[rs.idx]);
                 rs.next();
-                issued = j + 1;
+                issued = st + 1;
             }
             // No copy may still be landing in shared memory when the CTA exits: wait for the
             // stages issued last (immediate on the normal path, bounded on an error path).
-            for (int j = max(0, issued - kStages); j < issued; j++)
-                mbar_wait(&full[j % kStages], (j / kStages) & 1);
+            for (int st = max(0, issued - kStages); st < issued; st++)
+                mbar_wait(&full[st % kStages], (st / kStages) & 1);
         }
     } else if (warp >= 5 && warp < 5 + kIssuers) {
-        // ---------------- MMA issue: warp 5 + i issues the steps j = i (mod kIssuers) ----------
-        // Several issuers share the per-step cost of barrier waits, MMA issue and commits;
-        // their MMAs touch disjoint stages and accumulators.
+        // ---------------- MMA issue: warp 5 + i issues the stages st = i (mod 2) ----------------
+        // Issuer i owns accumulators 2i and 2i + 1 (steps 2st and 2st + 1).
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(kTileM, kTileN);
+            const int i = warp - 5;
             const uint32_t sbase = smem_u32(gsm);
-            for (int j = warp - 5; j < nK32; j += kIssuers) {
-                const int s = j & (kStages - 1), b = j & (kAccBufs - 1);
-                if (!wait_or_report(&full[s], (uint32_t)(j / kStages) & 1u, p.err)) break;
-                if (!wait_or_report(&tempty[b], ((uint32_t)(j / kAccBufs) & 1u) ^ 1u, p.err)) break;
-                tc_fence_after();
+            for (int st = i; st < nst; st += kIssuers) {
+                const int s = st & (kStages - 1);
+                if (!wait_or_report(&full[s], (uint32_t)(st / kStages) & 1u, p.err)) break;
+                const uint32_t tph = ((uint32_t)(st / kIssuers) & 1u) ^ 1u;
                 const uint32_t sa = sbase + (uint32_t)(s * kStageBytes);
-                const uint64_t ad = smem_desc(sa), bd = smem_desc(sa + kTileBytes);
-                const uint32_t d = tmem + (uint32_t)(b * kTileN);
-                mma_f16(d, ad, bd, idesc, 0u);
-                mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);
+                bool ok = true;
+#pragma unroll
+                for (int t = 0; t < 2; t++) {
+                    const int b = 2 * i + t;
+                    if (!wait_or_report(&tempty[b], tph, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc(sa + t * kTileBytes);
+                    const uint64_t bd = smem_desc(sa + (2 + t) * kTileBytes);
+                    const uint32_t d = tmem + (uint32_t)(b * kTileN);
+                    mma_f16(d, ad, bd, idesc, 0u);
+                    mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);
+                }
+                if (!ok) break;
                 mma_commit(&empty[s]);
-                mma_commit(&tfull[b]);
             }
             // Every MMA issued has completed before tensor memory is released.
             mma_commit(&mma_done);
@@ -333,56 +349,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
         const bool mvalid = m < p.M;
         const int col0 = g * 64;
         const uint16_t *drow = p.d + (mvalid ? m : 0) * (int64_t)nK32;
-        const bool dvec = (nK32 & 7) == 0;  // rows of d are 16-byte aligned
-        // The activation scales of 8 consecutive steps, loaded one group ahead.
-        auto load_dx8 = [&](int j) -> uint4 {
-            if (!mvalid || j >= nK32) return make_uint4(0, 0, 0, 0);
-            if (dvec) return *reinterpret_cast<const uint4 *>(drow + j);
-            uint32_t v[4];
-#pragma unroll
-            for (int t = 0; t < 4; t++)
-                v[t] = (j + 2 * t < nK32) ? *reinterpret_cast<const uint32_t *>(drow + j + 2 * t)
-                                          : 0u;
-            return make_uint4(v[0], v[1], v[2], v[3]);
-        };
         uint64_t acc[32];
 #pragma unroll
         for (int c = 0; c < 32; c++) acc[c] = 0;
         bool first = true, ok = true;
         const uint32_t tlane = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)col0;
-        uint4 dq = load_dx8(0);
-        for (int j8 = 0; j8 < nK32 && ok; j8 += 8) {
-            const uint4 dcur = dq;
-            dq = load_dx8(j8 + 8);
+        // Activation scales of one stage (two fp16 in a word), loaded four stages ahead.
+        auto load_dx2 = [&](int st) -> uint32_t {
+            return (mvalid && st < nst) ? *reinterpret_cast<const uint32_t *>(drow + 2 * st) : 0u;
+        };
+        uint32_t dr[4];
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
-                const int j = j8 + i;
-                if (j >= nK32) break;
-                const int b = j & (kAccBufs - 1);
-                const uint32_t dw = i < 2 ? dcur.x : i < 4 ? dcur.y : i < 6 ? dcur.z : dcur.w;
-                const uint32_t dxb =
-                    __float_as_uint(f16_bits_to_float((uint16_t)((i & 1) ? (dw >> 16) : dw)));
-                const uint64_t dx2 = ((uint64_t)dxb << 32) | dxb;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&tfull[b], (uint32_t)(j / kAccBufs) & 1u))) {
+        for (int h = 0; h < 4; h++) dr[h] = load_dx2(h);
+        Ring<kStages> rs;
+        for (int st0 = 0; st0 < nst && ok; st0 += 4) {
+#pragma unroll
+            for (int h = 0; h < 4; h++) {
+                const int st = st0 + h;
+                if (st >= nst) break;
+                const uint32_t dw = dr[h];
+                dr[h] = load_dx2(st + 4);
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase))) {
                     if (lane == 0) atomicOr(p.err, 1);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tlane + (uint32_t)(b * kTileN);
-                uint64_t r[16];
-                tmem_ld32_pairs(taddr, r);
 #pragma unroll
-                for (int c = 0; c < 16; c++) ffma2p(acc[c], r[c], dx2);
-                tmem_ld32_pairs(taddr + 32, r);
-                // The accumulator is free once both halves are in registers.
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[b]);
+                for (int t = 0; t < 2; t++) {
+                    const int b = (2 * st + t) & (kAccBufs - 1);
+                    const uint32_t dxb =
+                        __float_as_uint(f16_bits_to_float((uint16_t)(t ? (dw >> 16) : dw)));
+                    const uint64_t dx2 = ((uint64_t)dxb << 32) | dxb;
+                    const uint32_t taddr = tlane + (uint32_t)(b * kTileN);
+                    uint64_t r[16];
+                    tmem_ld32_pairs(taddr, r);
 #pragma unroll
-                for (int c = 0; c < 16; c++) ffma2p(acc[16 + c], r[c], dx2);
-                if ((j + 1) % kSeg == 0 || j + 1 == nK32) {
+                    for (int c = 0; c < 16; c++) ffma2p(acc[c], r[c], dx2);
+                    tmem_ld32_pairs(taddr + 32, r);
+                    // The accumulator is free once both halves are in registers.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[b]);
+#pragma unroll
+                    for (int c = 0; c < 16; c++) ffma2p(acc[16 + c], r[c], dx2);
+                }
+                rs.next();
+                if ((2 * st + 2) % kSeg == 0 || st + 1 == nst) {
                     float *t = tot + col0 * kTotPitch + mrow;
 #pragma unroll
                     for (int c = 0; c < 32; c++) {
