@@ -41,7 +41,6 @@ constexpr int kStageBytes = 4 * kTileBytes;
 constexpr int kIssuers = 2;                      // MMA-issuing warps, alternating stages
 constexpr int kAccBufs = 4;                      // tensor-memory accumulators (128 columns each)
 constexpr int kSeg = 32;                         // K32 blocks per drain segment
-constexpr int kWin = 8;                          // K32 blocks per expander prefetch window
 constexpr int kTotPitch = kTileM + 1;            // totals [n][m] pitch (conflict-free both ways)
 constexpr int kTotBytes = kTileN * kTotPitch * 4;
 constexpr int kTotOffset = kStages * kStageBytes;
@@ -208,79 +207,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
 
     if (warp < 4) {
         // ---------------- weight expanders: thread = weight row ----------------
-        // Packed weights are read straight from global memory one window (8 K32 blocks) ahead.
+        // The packed weights and scale of each stage are read from global memory kQ stages
+        // ahead into a small register queue.
+        constexpr int kQ = 4;
         const int nl = threadIdx.x;
         const int64_t n = n0 + nl;
         const bool valid = n < p.N;
         const int64_t nn = valid ? n : 0;
-        constexpr int kBlkBytes = F == kG2 ? 8 : 4;       // packed bytes per K32 block and row
-        constexpr int kVec = kWin * kBlkBytes / 16;        // uint4 per window
-        const uint8_t *row = p.bits + nn * (int64_t)nK32 * kBlkBytes;
+        constexpr int kStBytes = F == kG2 ? 16 : 8;       // packed bytes per stage and row
+        const uint8_t *row = p.bits + nn * (int64_t)nst * kStBytes;
         const uint16_t *srow = p.scales + nn * (int64_t)p.S;
-        const int nwin = (nK32 + kWin - 1) / kWin;
-        auto load_window = [&](int w, uint4 (&cw)[kVec], uint2 &sc) {
-            const int j = w * kWin;
-#pragma unroll
-            for (int v = 0; v < kVec; v++) {
-                const int jv = j + v * (16 / kBlkBytes);
-                cw[v] = (valid && jv < nK32)
-                            ? *reinterpret_cast<const uint4 *>(row + (int64_t)jv * kBlkBytes)
-                            : make_uint4(0, 0, 0, 0);
+        // Q2_0_g64: a stage is one 64-weight block (16 code bytes, one scale); Q1_0: half of a
+        // 128-weight block (8 sign bytes; the scale of block st / 2).
+        auto load_stage = [&](int st, uint4 &c, uint32_t &sc) {
+            if (!valid || st >= nst) {
+                c = make_uint4(0, 0, 0, 0);
+                sc = 0;
+            } else if (F == kG2) {
+                c = *reinterpret_cast<const uint4 *>(row + (int64_t)st * 16);
+                sc = srow[st];
+            } else {
+                const uint2 v = *reinterpret_cast<const uint2 *>(row + (int64_t)st * 8);
+                c = make_uint4(v.x, v.y, 0, 0);
+                sc = srow[st >> 1];
             }
-            // Scales of the window's weight blocks (4 for Q2_0_g64, 2 for Q1_0); the scale rows
-            // are padded with zeros to a multiple of 8 entries, so these loads stay in the row.
-            if (F == kG2)
-                sc = (valid && j < nK32) ? *reinterpret_cast<const uint2 *>(srow + j / 2)
-                                         : make_uint2(0, 0);
-            else
-                sc = make_uint2((valid && j < nK32)
-                                    ? *reinterpret_cast<const uint32_t *>(srow + j / 4) : 0u,
-                                0u);
         };
-        uint4 cur[kVec], nxt[kVec];
-        uint2 cs, ns = make_uint2(0, 0);
-        load_window(0, cur, cs);
+        uint4 qc[kQ];
+        uint32_t qs[kQ];
+#pragma unroll
+        for (int i = 0; i < kQ; i++) load_stage(i, qc[i], qs[i]);
         const uint32_t boff = (uint32_t)canon_offset(nl, 0) + 2 * kTileBytes;
         Ring<kStages> rs;
-        bool ok = true;
-        for (int w = 0; w < nwin && ok; w++) {
-            if (w + 1 < nwin) load_window(w + 1, nxt, ns);
+        for (int st = 0; st < nst; st++) {
+            const uint4 cw = qc[0];
+            const uint32_t sc = qs[0];
 #pragma unroll
-            for (int h = 0; h < kWin / 2; h++) {  // one stage = K32 blocks 2h, 2h + 1 of the window
-                if (w * kWin + 2 * h >= nK32) break;
-                if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase ^ 1u))) {
-                    if (lane == 0) atomicOr(p.err, 1);
-                    ok = false;
-                    break;
-                }
-                uint8_t *bt = gsm + rs.idx * kStageBytes + boff;
-#pragma unroll
-                for (int t = 0; t < 2; t++) {
-                    const int i = 2 * h + t;
-                    uint4 c[4];
-                    if (F == kG2) {
-                        const uint4 &v = cur[i / 2];
-                        const uint32_t sw = (i / 4) ? cs.y : cs.x;
-                        const uint16_t sb = (uint16_t)(((i / 2) & 1) ? (sw >> 16) : (sw & 0xFFFFu));
-                        expand_q2((i & 1) ? v.z : v.x, (i & 1) ? v.w : v.y, __ushort_as_half(sb), c);
-                    } else {
-                        const uint4 &v = cur[i / 4];
-                        const uint32_t ww =
-                            (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
-                        expand_q1(ww, (uint16_t)((i / 4) ? (cs.x >> 16) : (cs.x & 0xFFFFu)), c);
-                    }
-#pragma unroll
-                    for (int kc = 0; kc < 4; kc++)
-                        *reinterpret_cast<uint4 *>(bt + t * kTileBytes + kc * kCoreLBO) = c[kc];
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[rs.idx]);
-                rs.next();
+            for (int i = 0; i + 1 < kQ; i++) {
+                qc[i] = qc[i + 1];
+                qs[i] = qs[i + 1];
             }
+            load_stage(st + kQ, qc[kQ - 1], qs[kQ - 1]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase ^ 1u))) {
+                if (lane == 0) atomicOr(p.err, 1);
+                break;
+            }
+            uint8_t *bt = gsm + rs.idx * kStageBytes + boff;
 #pragma unroll
-            for (int v = 0; v < kVec; v++) cur[v] = nxt[v];
-            cs = ns;
+            for (int t = 0; t < 2; t++) {
+                uint4 c[4];
+                if (F == kG2)
+                    expand_q2(t ? cw.z : cw.x, t ? cw.w : cw.y, __ushort_as_half((uint16_t)sc), c);
+                else
+                    expand_q1(t ? cw.y : cw.x, (uint16_t)sc, c);
+#pragma unroll
+                for (int kc = 0; kc < 4; kc++)
+                    *reinterpret_cast<uint4 *>(bt + t * kTileBytes + kc * kCoreLBO) = c[kc];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[rs.idx]);
+            rs.next();
         }
     } else if (warp == 4) {
         // ---------------- activation tiles: one 16 KB bulk copy per stage ----------------
@@ -352,62 +338,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
         uint64_t acc[32];
 #pragma unroll
         for (int c = 0; c < 32; c++) acc[c] = 0;
-        bool first = true, ok = true;
+        bool first = true;
         const uint32_t tlane = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)col0;
-        // Activation scales of one stage (two fp16 in a word), loaded four stages ahead.
+        // Activation scales of one stage (two fp16 in a word), loaded three stages ahead.
         auto load_dx2 = [&](int st) -> uint32_t {
             return (mvalid && st < nst) ? *reinterpret_cast<const uint32_t *>(drow + 2 * st) : 0u;
         };
-        uint32_t dr[4];
-#pragma unroll
-        for (int h = 0; h < 4; h++) dr[h] = load_dx2(h);
+        uint32_t dq0 = load_dx2(0), dq1 = load_dx2(1), dq2 = load_dx2(2);
         Ring<kStages> rs;
-        for (int st0 = 0; st0 < nst && ok; st0 += 4) {
+        for (int st = 0; st < nst; st++) {
+            const uint32_t dw = dq0;
+            dq0 = dq1;
+            dq1 = dq2;
+            dq2 = load_dx2(st + 3);
+            if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase))) {
+                if (lane == 0) atomicOr(p.err, 1);
+                break;
+            }
+            tc_fence_after();
 #pragma unroll
-            for (int h = 0; h < 4; h++) {
-                const int st = st0 + h;
-                if (st >= nst) break;
-                const uint32_t dw = dr[h];
-                dr[h] = load_dx2(st + 4);
-                if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase))) {
-                    if (lane == 0) atomicOr(p.err, 1);
-                    ok = false;
-                    break;
+            for (int t = 0; t < 2; t++) {
+                const int b = (2 * st + t) & (kAccBufs - 1);
+                const uint32_t dxb =
+                    __float_as_uint(f16_bits_to_float((uint16_t)(t ? (dw >> 16) : dw)));
+                const uint64_t dx2 = ((uint64_t)dxb << 32) | dxb;
+                const uint32_t taddr = tlane + (uint32_t)(b * kTileN);
+                uint64_t r[16];
+                tmem_ld32_pairs(taddr, r);
+#pragma unroll
+                for (int c = 0; c < 16; c++) ffma2p(acc[c], r[c], dx2);
+                tmem_ld32_pairs(taddr + 32, r);
+                // The accumulator is free once both halves are in registers.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);
+#pragma unroll
+                for (int c = 0; c < 16; c++) ffma2p(acc[16 + c], r[c], dx2);
+            }
+            rs.next();
+            if ((2 * st + 2) % kSeg == 0 || st + 1 == nst) {
+                float *t = tot + col0 * kTotPitch + mrow;
+#pragma unroll
+                for (int c = 0; c < 32; c++) {
+                    const float lo = __uint_as_float((uint32_t)acc[c]);
+                    const float hi = __uint_as_float((uint32_t)(acc[c] >> 32));
+                    float *t0 = t + (2 * c) * kTotPitch, *t1 = t0 + kTotPitch;
+                    *t0 = first ? lo : *t0 + lo;
+                    *t1 = first ? hi : *t1 + hi;
+                    acc[c] = 0;
                 }
-                tc_fence_after();
-#pragma unroll
-                for (int t = 0; t < 2; t++) {
-                    const int b = (2 * st + t) & (kAccBufs - 1);
-                    const uint32_t dxb =
-                        __float_as_uint(f16_bits_to_float((uint16_t)(t ? (dw >> 16) : dw)));
-                    const uint64_t dx2 = ((uint64_t)dxb << 32) | dxb;
-                    const uint32_t taddr = tlane + (uint32_t)(b * kTileN);
-                    uint64_t r[16];
-                    tmem_ld32_pairs(taddr, r);
-#pragma unroll
-                    for (int c = 0; c < 16; c++) ffma2p(acc[c], r[c], dx2);
-                    tmem_ld32_pairs(taddr + 32, r);
-                    // The accumulator is free once both halves are in registers.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[b]);
-#pragma unroll
-                    for (int c = 0; c < 16; c++) ffma2p(acc[16 + c], r[c], dx2);
-                }
-                rs.next();
-                if ((2 * st + 2) % kSeg == 0 || st + 1 == nst) {
-                    float *t = tot + col0 * kTotPitch + mrow;
-#pragma unroll
-                    for (int c = 0; c < 32; c++) {
-                        const float lo = __uint_as_float((uint32_t)acc[c]);
-                        const float hi = __uint_as_float((uint32_t)(acc[c] >> 32));
-                        float *t0 = t + (2 * c) * kTotPitch, *t1 = t0 + kTotPitch;
-                        *t0 = first ? lo : *t0 + lo;
-                        *t1 = first ? hi : *t1 + hi;
-                        acc[c] = 0;
-                    }
-                    first = false;
-                }
+                first = false;
             }
         }
         // All eight drain warps are done with the totals: store the tile, one 128-byte row
