@@ -169,7 +169,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------------
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for name in ("lb_stream.cuh", "lb_gemv_q.cu", "lb_common.cuh"):
+    for name in ("lb_stream.cuh", "lb_gemv_q.cuh", "lb_gemv_q2.cu", "lb_common.cuh"):
         with open(os.path.join(ROOT, "bit_matvec_lb_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
