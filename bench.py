@@ -1,6 +1,7 @@
 """Benchmark of the GB300 low-bit product library.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
+                    [--rows-only decode|prefill]
 
 Headline workload (the decode GEMV the metric is quoted on): Q2_0_g64 GEMV, 4096 x 4096 weights,
 batch 1, q8_0 activations.  One step = one pass of the decode hot path over one token: q8_0
@@ -403,12 +404,22 @@ def headline(lb, args, dist, out):
 # ---------------------------------------------------------------------------------------------
 # other rows of the hot path (outside the headline timed region)
 # ---------------------------------------------------------------------------------------------
-def rows_measure(lb, out):
+def rows_measure(lb, out, which: str = "all"):
+    import torch
+    import synth
+    stream = torch.cuda.Stream()
+    rows = {}
+    if which in ("all", "decode"):
+        rows_decode(lb, rows, stream)
+    if which in ("all", "prefill"):
+        rows_prefill(lb, rows, stream)
+    out["rows"] = rows
+
+
+def rows_decode(lb, rows, stream):
     import torch
     import synth
     hbm, _ = peaks()
-    stream = torch.cuda.Stream()
-    rows = {}
 
     # (1) config 2 at batch 8
     N, K, B = ROWS_N, ROWS_K, 8
@@ -513,6 +524,11 @@ def rows_measure(lb, out):
             "ms_per_token": round(ms, 4), "bytes": tot,
             "head_GB/s": round(HN * HK * 2 / (ms_head * 1e-3) / 1e9, 1),
             "body_GB/s": round(body_bytes / ((ms - ms_head) * 1e-3) / 1e9, 1)}
+
+
+def rows_prefill(lb, rows, stream):
+    import torch
+    import synth
     # (4) Qwen3-8B-shaped prefill: 512 tokens through one layer's seven projections, Q1_0 and
     #     Q2_0_g64 (q8_0 quantization of the three distinct activations + seven GEMMs per pass)
     M = synth.PREFILL_M
@@ -543,7 +559,6 @@ def rows_measure(lb, out):
                     f"exact f16 tensor-core path the GEMM runs on"}
         del proj, ys
         torch.cuda.empty_cache()
-    out["rows"] = rows
 
 
 # ---------------------------------------------------------------------------------------------
@@ -586,6 +601,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true")
+    ap.add_argument("--rows-only", choices=["decode", "prefill"], default=None,
+                    help="skip the headline; run (and print) only these rows")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -612,6 +629,12 @@ def main():
     if dist.world == 1:
         torch.cuda.set_device(0)
     lb.load()
+    if args.rows_only:
+        out = {}
+        rows_measure(lb, out, args.rows_only)
+        print(json.dumps(out))
+        dist.close()
+        return
     out = dict(base)
     headline(lb, args, dist, out)
     if dist.rank == 0 and dist.world == 1 and not args.no_rows:
