@@ -483,11 +483,260 @@ inline int launch_stream_cfg(StreamParams &p, const StreamPlan &pl, int sms, cud
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kStreamThreads), (size_t)pl.smem, st, p);
 }
 
+// ------------------------------------------------------------------------------------------
+// Batched variant (B >= 3): lane = weight row.
+//
+// At larger batch the activation reads, not the weights, bound the kernel above: every lane
+// reads the activation words of its own chunk, once per token and row.  Here a warp takes 32
+// rows, one per lane, and a contiguous range of the row's chunks, so for any chunk all 32 lanes
+// read the same activation words -- shared-memory broadcasts -- and each weight chunk is read
+// once.  A unit is 32 rows; the eight consumer warps split its chunks and add their partial sums
+// through shared memory at the end of the unit.  Rows are staged one bulk copy per row (one per
+// producer lane) with a 16-byte pad, so the lanes' 16-byte weight reads do not conflict.
+// ------------------------------------------------------------------------------------------
+constexpr int kRowsPerUnit = 32;
+
+template <int F, int B>
+__global__ void __launch_bounds__(kStreamThreads, 2)
+    stream_rows_kernel(const __grid_constant__ StreamParams p) {
+    constexpr int kCols = FmtInfo<F>::kCols;
+    constexpr int kPer = kCols / 32;
+    constexpr int TR = kRowsPerUnit;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kMaxStages;
+    uint8_t *act = smem + kBarBytes;
+    uint8_t *stages = act + p.act_bytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KC = p.KC;                  // chunks per stage (a multiple of 8, or the whole row)
+    const int KCp = (KC + 7) & ~7;
+    const int wpitch = (KC + 1) * 16;     // padded row pitch of the weight slice
+    const int spitch = KCp * 2;           // row pitch of the scale slice
+    const int nq8 = (int)(p.K / 32);
+    float *red = reinterpret_cast<float *>(stages + (size_t)p.stages * p.stage_bytes);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer warp: lane r copies row r of every stage ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        int mi = 0;
+        for (int u = blockIdx.x; u < p.nunits && ok; u += gridDim.x) {
+            mi = find_mat(p, u, mi);
+            const StreamMat &M = p.m[mi];
+            const int row0 = (u - M.unit0) * TR;
+            const int rows = min(TR, M.N - row0);
+            for (int ct = 0; ct < p.nct; ct++) {
+                const int c0 = ct * KC;
+                const int kc = min(KC, p.nchunk - c0);
+                const int kcp = (kc + 7) & ~7;
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *sb = stages + (size_t)stage * p.stage_bytes;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(
+                        &full[stage], (uint32_t)(rows * (kc * 16 + (F != kTrit ? kcp * 2 : 0))));
+                __syncwarp();
+                if (lane < rows) {
+                    const int64_t row = row0 + lane;
+                    bulk_g2s(sb + (size_t)lane * wpitch, M.w + (row * p.nchunk + c0) * 16,
+                             (uint32_t)kc * 16, &full[stage]);
+                    if (F != kTrit)
+                        bulk_g2s(sb + (size_t)TR * wpitch + (size_t)lane * spitch,
+                                 M.scales + row * p.S + c0, (uint32_t)kcp * 2, &full[stage]);
+                }
+                issued++;
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok && lane == 0) report(p.err);
+        for (int i = max(0, issued - p.stages); i < issued; i++)
+            mbar_wait(&full[i % p.stages], (uint32_t)((i / p.stages) & 1));
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    pdl_wait();
+    uint4 *xp = reinterpret_cast<uint4 *>(act);
+    float2 *st = reinterpret_cast<float2 *>(act + (size_t)B * p.K);
+    stage_activations<F>(p.q, p.d, B, p.K, xp, st, threadIdx.x, kConsumerThreads);
+    named_sync(1, kConsumerThreads);
+
+    int stage = 0;
+    uint32_t phase = 0;
+    int mi = 0;
+    const int tok_quads = (int)(p.K / 16);
+    for (int u = blockIdx.x; u < p.nunits; u += gridDim.x) {
+        mi = find_mat(p, u, mi);
+        const StreamMat &M = p.m[mi];
+        const int row0 = (u - M.unit0) * TR;
+        const int rows = min(TR, M.N - row0);
+        typedef typename std::conditional<F == kTrit, int, float>::type Acc;
+        Acc acc[B];
+#pragma unroll
+        for (int b = 0; b < B; b++) acc[b] = 0;
+
+        for (int ct = 0; ct < p.nct; ct++) {
+            const int c0 = ct * KC;
+            const int kc = min(KC, p.nchunk - c0);
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
+                if (lane == 0) report(p.err);
+                return;
+            }
+            const uint8_t *sb = stages + (size_t)stage * p.stage_bytes;
+            const uint8_t *wrow = sb + (size_t)lane * wpitch;
+            const uint16_t *srow =
+                reinterpret_cast<const uint16_t *>(sb + (size_t)TR * wpitch + (size_t)lane * spitch);
+            // this warp's chunks of the stage: a contiguous eighth (rounded up)
+            const int per = (kc + kConsumerWarps - 1) / kConsumerWarps;
+            const int cb = warp * per, ce = min(kc, cb + per);
+            for (int c = cb; c < ce; c++) {
+                const int cg = c0 + c;
+                const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + (size_t)c * 16);
+                const float dw = F != kTrit ? f16_bits_to_float(srow[c]) : 0.0f;
+#pragma unroll
+                for (int b = 0; b < B; b++) {
+                    const uint4 *tok = xp + b * tok_quads;
+                    if (F == kTrit) {
+#pragma unroll
+                        for (int h = 0; h < 2; h++) {
+                            const uint4 a0 = tok[quad_slot<F>(cg, 2 * h)];
+                            const uint4 a1 = tok[quad_slot<F>(cg, 2 * h + 1)];
+                            const int vp = q1_word_dot(h ? wv.y : wv.x, a0, a1, 0);
+                            const int vn = q1_word_dot(h ? wv.w : wv.z, a0, a1, 0);
+                            acc[b] += (Acc)((vp - vn) >> 7);
+                        }
+                    } else {
+                        const float2 *stb = st + b * nq8 + cg * kPer;
+                        float t = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < kPer; j++) {
+                            const float2 ds = stb[j];  // {d / 64, -64 * sum q}
+                            const int s64 = __float_as_int(ds.y);
+                            const uint4 av0 = tok[quad_slot<F>(cg, 2 * j)];
+                            const uint4 av1 = tok[quad_slot<F>(cg, 2 * j + 1)];
+                            const int a = F == kQ1
+                                              ? q1_word_dot(word_of(wv, j), av0, av1, s64)
+                                              : q2_block_dot(word_of(wv, 2 * j),
+                                                             word_of(wv, 2 * j + 1), av0, av1,
+                                                             s64);
+                            t = fmaf(ds.x, (float)a, t);
+                        }
+                        acc[b] = fmaf(dw, t, acc[b]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+        // add the eight warps' partial sums of this unit's rows
+#pragma unroll
+        for (int b = 0; b < B; b++)
+            red[(warp * B + b) * TR + lane] = F == kTrit ? __int_as_float((int)acc[b])
+                                                         : (float)acc[b];
+        named_sync(1, kConsumerThreads);
+        for (int i = threadIdx.x; i < B * TR; i += kConsumerThreads) {
+            const int b = i / TR, r = i % TR;
+            if (r < rows) {
+                const int64_t o = (int64_t)b * M.N + row0 + r;
+                if (F == kTrit) {
+                    int a = 0;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; w++)
+                        a += __float_as_int(red[(w * B + b) * TR + r]);
+                    const float t = __fmul_rn((float)a, p.x_scale[b]);
+                    M.y[o] = __fmul_rn(t, M.w_scale);
+                    if (M.aux) M.aux[o] = a;
+                } else {
+                    float v = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; w++) v += red[(w * B + b) * TR + r];
+                    M.y[o] = v;
+                }
+            }
+        }
+        named_sync(1, kConsumerThreads);
+    }
+}
+
+// Geometry of the batched variant: chunks per stage (whole row, or a multiple of 8 within a
+// 40 KB stage), stage count for two CTAs per SM where possible.
+inline StreamPlan plan_rows(int F, int B, int64_t K) {
+    const int cols = F == kQ1 ? 128 : 64;
+    const int nchunk = (int)(K / cols);
+    const int scale_b = F == kTrit ? 0 : 2;
+    StreamPlan pl{};
+    pl.act_bytes = (int)(((int64_t)B * K + (F == kTrit ? 0 : (int64_t)B * (K / 32) * 8) + 127) /
+                         128 * 128);
+    auto stage_cost = [&](int kc) {
+        return kRowsPerUnit * ((kc + 1) * 16 + ((kc + 7) & ~7) * scale_b);
+    };
+    int KC = nchunk;
+    if (stage_cost(KC) > 40 * 1024) KC = (40 * 1024 / kRowsPerUnit - 16) / (16 + scale_b) / 8 * 8;
+    pl.RW = 0;
+    pl.KC = KC;
+    pl.nct = (nchunk + KC - 1) / KC;
+    pl.stage_bytes = (stage_cost(KC) + 127) / 128 * 128;
+    const int red_bytes = kConsumerWarps * B * kRowsPerUnit * 4;
+    const int per_cta = 113 * 1024;
+    int stages = kMaxStages;
+    while (stages > 2 && kBarBytes + pl.act_bytes + stages * pl.stage_bytes + red_bytes > per_cta)
+        stages--;
+    pl.stages = stages;
+    pl.smem = kBarBytes + pl.act_bytes + stages * pl.stage_bytes + red_bytes;
+    return pl;
+}
+
+template <int F, int B>
+inline int launch_rows(StreamParams &p, int sms, cudaStream_t st) {
+    const StreamPlan pl = plan_rows(F, B, p.K);
+    auto kern = stream_rows_kernel<F, B>;
+    int bps = 0;
+    if (int e = prepare_kernel(reinterpret_cast<const void *>(kern), kStreamThreads,
+                               (size_t)pl.smem, &bps))
+        return e;
+    int units = 0;
+    for (int i = 0; i < p.G; i++) {
+        p.m[i].unit0 = units;
+        units += (p.m[i].N + kRowsPerUnit - 1) / kRowsPerUnit;
+    }
+    p.nunits = units;
+    p.nct = pl.nct;
+    p.KC = pl.KC;
+    p.stages = pl.stages;
+    p.stage_bytes = pl.stage_bytes;
+    p.act_bytes = pl.act_bytes;
+    int64_t grid = (int64_t)sms * bps;
+    if (grid > units) grid = units;
+    if (grid < 1) grid = 1;
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kStreamThreads), (size_t)pl.smem, st, p);
+}
+
 template <int F, int B>
 inline int launch_stream(StreamParams &p, bool aux, int sms, cudaStream_t st) {
     if (aux) return launch_stream_cfg<F, B, 1, true>(p, plan_stream(F, B, p.K, 1), sms, st);
     if constexpr (B > 2) {
-        return launch_stream_cfg<F, B, 1, false>(p, plan_stream(F, B, p.K, 1), sms, st);
+        return launch_rows<F, B>(p, sms, st);
     } else {
         const StreamPlan pl = plan_stream(F, B, p.K, 4);
         if (pl.RW == 4) return launch_stream_cfg<F, B, 4, false>(p, pl, sms, st);

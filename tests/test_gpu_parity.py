@@ -345,3 +345,31 @@ def test_grouped_trit(B):
 
 def test_device_status_clean():
     assert lb.lb_device_status() == 0
+
+
+@pytest.mark.parametrize("qk", [128, 64])
+@pytest.mark.parametrize("B", [3, 5, 8])
+def test_q_batched_ragged_production(qk, B):
+    """Batch 3..8 without the block-sum hook (the lane-per-row kernel): ragged row count (not a
+    multiple of 32), long rows sliced into several stages, and short rows."""
+    for N, K in ((77, 1024 if qk == 128 else 320), (45, 12288)):
+        blocks = synth.q1_0_blocks(N, K, seed=600 + B) if qk == 128 else synth.q2_0_blocks(
+            N, K, seed=600 + B, probs=(0.25, 0.25, 0.25, 0.25))
+        q, dx = _q8(B, K, seed=610 + B)
+        ref = (oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product)(blocks, q, dx)
+        y, _ = gemv_q(qk, blocks, q, dx, want_isum=False)
+        assert within(y, ref.y_exact, ref.mag)[0]
+
+
+@pytest.mark.parametrize("B", [3, 8])
+def test_trit_batched_ragged(B):
+    """Planar at batch 3..8 (lane-per-row kernel): bit-exact accumulators and outputs, ragged
+    rows, a sliced long row."""
+    for N, K in ((77, 2560), (33, 6912)):
+        planes, _ = synth.trit_planes(N, K, seed=620 + B)
+        x = synth.activations(B, K, seed=630 + B)
+        qi, xs = oracle.quantize_i8_absmax(x)
+        acc_ref, y_ref = oracle.trit_planes_product(planes, 0.0173, qi, xs)
+        acc, y = gemv_trit(planes, 0.0173, qi, xs)
+        assert np.array_equal(acc, acc_ref)
+        assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
