@@ -691,19 +691,24 @@ inline StreamPlan plan_rows(int F, int B, int64_t K) {
     auto stage_cost = [&](int kc) {
         return kRowsPerUnit * ((kc + 1) * 16 + ((kc + 7) & ~7) * scale_b);
     };
+    const int red_b = kConsumerWarps * B * kRowsPerUnit * 4;
+    // Stage budget: two stages next to the activation image should still let two CTAs share
+    // an SM (up to 40 KB per stage, at least 8 KB).
+    int budget = (113 * 1024 - kBarBytes - pl.act_bytes - red_b) / 2;
+    if (budget < 8 * 1024) budget = 40 * 1024;  // one CTA per SM anyway: large stages
+    if (budget > 40 * 1024) budget = 40 * 1024;
     int KC = nchunk;
-    if (stage_cost(KC) > 40 * 1024) KC = (40 * 1024 / kRowsPerUnit - 16) / (16 + scale_b) / 8 * 8;
+    if (stage_cost(KC) > budget) KC = (budget / kRowsPerUnit - 16) / (16 + scale_b) / 8 * 8;
     pl.RW = 0;
     pl.KC = KC;
     pl.nct = (nchunk + KC - 1) / KC;
     pl.stage_bytes = (stage_cost(KC) + 127) / 128 * 128;
-    const int red_bytes = kConsumerWarps * B * kRowsPerUnit * 4;
     const int per_cta = 113 * 1024;
     int stages = kMaxStages;
-    while (stages > 2 && kBarBytes + pl.act_bytes + stages * pl.stage_bytes + red_bytes > per_cta)
+    while (stages > 2 && kBarBytes + pl.act_bytes + stages * pl.stage_bytes + red_b > per_cta)
         stages--;
     pl.stages = stages;
-    pl.smem = kBarBytes + pl.act_bytes + stages * pl.stage_bytes + red_bytes;
+    pl.smem = kBarBytes + pl.act_bytes + stages * pl.stage_bytes + red_b;
     return pl;
 }
 
