@@ -7,6 +7,8 @@
 // tritium.technology "Architecture", section 4.2).
 #include "lb_common.cuh"
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 #include <unordered_map>
 
@@ -112,6 +114,36 @@ int prepare_kernel(const void *kernel, int threads, size_t smem, int *blocks_per
     }
     *blocks_per_sm = p.blocks_per_sm;
     return p.blocks_per_sm >= 1 ? LB_OK : LB_ERR_SHAPE;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+static std::mutex g_encode_mutex;
+
+int encode_rows_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows,
+                    uint32_t box_bytes, uint32_t box_rows) {
+    {
+        std::lock_guard<std::mutex> lock(g_encode_mutex);
+        if (!g_encode_tiled) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q{};
+            const cudaError_t e = cudaGetDriverEntryPointByVersion(
+                "cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+                record_cuda_error(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
+                return LB_ERR_LAUNCH;
+            }
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    const cuuint64_t dims[2] = {row_bytes, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_bytes, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base),
+                                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LB_OK : LB_ERR_LAUNCH;
 }
 
 }  // namespace lb

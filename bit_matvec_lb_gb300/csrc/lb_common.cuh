@@ -1,6 +1,7 @@
 // lb_common.cuh -- shared host checks and device helpers of the GB300 low-bit library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -34,6 +35,11 @@ int *device_error_word();
 int prepare_kernel(const void *kernel, int threads, size_t smem, int *blocks_per_sm);
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Tensor map (TMA descriptor) of a row-major byte matrix [rows][row_bytes] whose copies are
+// boxes of box_rows x box_bytes; rows past the end read as zero.  LB_OK or LB_ERR_LAUNCH.
+int encode_rows_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows,
+                    uint32_t box_bytes, uint32_t box_rows);
 
 // Remember a failed CUDA call's error for lb_last_cuda_error() (calling thread) and clear it
 // from the runtime's last-error slot.
@@ -199,6 +205,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, limit_ns);
+}
+// 2-D tensor copy (box at column byte x, row y) global -> this CTA's shared memory, counted on
+// `bar`.  x must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
 }
 // Bulk copy global -> this CTA's shared memory; completion is counted on `bar` (tx bytes).
 // dst, src and bytes must be multiples of 16.

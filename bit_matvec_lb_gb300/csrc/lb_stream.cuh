@@ -750,8 +750,24 @@ inline int launch_stream(StreamParams &p, bool aux, int sms, cudaStream_t st) {
     }
 }
 
+template <int F, int B>
+inline int launch_tc_gemv(StreamParams &p, int sms, cudaStream_t st);
+
 template <int F>
 inline int dispatch_stream(StreamParams &p, int B, bool aux, int sms, cudaStream_t st) {
+    // Three or more tokens: the tensor-core variant (lb_tcgemv.cuh) when K is a multiple of
+    // its 256-column step and its activation operand (16 K bytes) fits in shared memory; the
+    // block-sum hook stays on the streaming kernels.
+    if (B >= 3 && !aux && p.K % 256 == 0 && p.K <= 4096) {
+        switch (B) {
+            case 3: return launch_tc_gemv<F, 3>(p, sms, st);
+            case 4: return launch_tc_gemv<F, 4>(p, sms, st);
+            case 5: return launch_tc_gemv<F, 5>(p, sms, st);
+            case 6: return launch_tc_gemv<F, 6>(p, sms, st);
+            case 7: return launch_tc_gemv<F, 7>(p, sms, st);
+            case 8: return launch_tc_gemv<F, 8>(p, sms, st);
+        }
+    }
     switch (B) {
         case 1: return launch_stream<F, 1>(p, aux, sms, st);
         case 2: return launch_stream<F, 2>(p, aux, sms, st);
@@ -768,3 +784,5 @@ inline int dispatch_stream(StreamParams &p, int B, bool aux, int sms, cudaStream
 inline int64_t scale_stride(int64_t K, int qk) { return (K / qk + 7) / 8 * 8; }
 
 }  // namespace lb
+
+#include "lb_tcgemv.cuh"
