@@ -120,7 +120,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 static std::mutex g_encode_mutex;
 
 int encode_rows_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows,
-                    uint32_t box_bytes, uint32_t box_rows) {
+                    uint32_t box_bytes, uint32_t box_rows, int swizzle_bytes) {
     {
         std::lock_guard<std::mutex> lock(g_encode_mutex);
         if (!g_encode_tiled) {
@@ -141,7 +141,10 @@ int encode_rows_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base),
                                       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                      swizzle_bytes == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                                      : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                            : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? LB_OK : LB_ERR_LAUNCH;
 }

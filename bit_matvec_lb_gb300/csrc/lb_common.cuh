@@ -37,9 +37,11 @@ int prepare_kernel(const void *kernel, int threads, size_t smem, int *blocks_per
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // Tensor map (TMA descriptor) of a row-major byte matrix [rows][row_bytes] whose copies are
-// boxes of box_rows x box_bytes; rows past the end read as zero.  LB_OK or LB_ERR_LAUNCH.
+// boxes of box_rows x box_bytes; rows past the end read as zero.  `swizzle_bytes` 0 (none), 32
+// or 64: the 16-byte chunks of each box row are XOR-permuted by the hardware's 32 B / 64 B
+// pattern.  LB_OK or LB_ERR_LAUNCH.
 int encode_rows_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows,
-                    uint32_t box_bytes, uint32_t box_rows);
+                    uint32_t box_bytes, uint32_t box_rows, int swizzle_bytes = 0);
 
 // Remember a failed CUDA call's error for lb_last_cuda_error() (calling thread) and clear it
 // from the runtime's last-error slot.

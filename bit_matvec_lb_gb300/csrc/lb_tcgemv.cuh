@@ -44,7 +44,8 @@ constexpr int kTgWStage = kTgBlocks * kTgWTile; // 32 KB
 constexpr int kTgXStage = kTgBlocks * kTgXTile; // 4 KB
 
 // Packed bytes of one row for one step, and the row pitch in the packed stage (dense: one
-// tensor copy per step lands the 128 rows back to back).
+// tensor copy per step lands the 128 rows back to back, with the hardware swizzle of a row's
+// size, 64 B or 32 B, so the decoders' 16-byte reads of 32 consecutive rows do not conflict).
 template <int F> struct TgFmt;
 template <> struct TgFmt<kQ1> { static constexpr int kBytes = kTgCols / 8; static constexpr int kPitch = kBytes; };
 template <> struct TgFmt<kQ2> { static constexpr int kBytes = kTgCols / 4; static constexpr int kPitch = kBytes; };
@@ -281,11 +282,13 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                 break;
             }
             const uint4 *src = reinterpret_cast<const uint4 *>(pst + pi * kTgRows * kPP + r * kPP);
+            // 16-byte chunk v of this row sits at chunk v ^ sw (the swizzle of the tensor copy)
+            const int sw = kPB == 64 ? ((r >> 1) & 3) : ((r >> 2) & 1);
             uint8_t *dst = wst + ai * kTgWStage + woff;
             if (F == kQ1) {
 #pragma unroll
                 for (int v = 0; v < kPB / 16; v++) {
-                    const uint4 c = src[v];
+                    const uint4 c = src[v ^ sw];
                     const uint32_t ws[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
                     for (int t = 0; t < 4; t++) {
@@ -299,7 +302,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             } else {
 #pragma unroll
                 for (int v = 0; v < kPB / 16; v++) {
-                    const uint4 c = src[v];  // Q2: blocks 2v, 2v+1; planar: one 64-column beat
+                    const uint4 c = src[v ^ sw];  // Q2: blocks 2v, 2v+1; planar: one 64-column beat
                     uint4 c0, c1;
                     if (F == kQ2) {
                         tg_decode_q2(c.x, c.y, c0, c1);
@@ -462,7 +465,8 @@ inline int launch_tc_gemv(StreamParams &p, int sms, cudaStream_t st) {
         units += (p.m[i].N + kTgRows - 1) / kTgRows;
         const uint64_t row_bytes = (uint64_t)p.nchunk * 16;
         if (int e = encode_rows_map(&maps.m[i], p.m[i].w, row_bytes, (uint64_t)p.m[i].N,
-                                    (uint32_t)TgFmt<F>::kBytes, (uint32_t)kTgRows))
+                                    (uint32_t)TgFmt<F>::kBytes, (uint32_t)kTgRows,
+                                    TgFmt<F>::kBytes))
             return e;
 
     }
