@@ -13,15 +13,15 @@
 // up with HBM; here a weight costs about half an instruction to decode and the products run on
 // the tensor cores.
 //
-// CTA (persistent, one per SM) = 12 warps working on units of 128 weight rows x all of K, in
+// CTA (persistent, one per SM) = 16 warps working on units of 128 weight rows x all of K, in
 // steps of 8 q8_0 blocks (256 columns).  The activation operand (hi/lo e4m3 tiles of all of K,
 // 16 K bytes) is built once per CTA by warps 1-11 and stays resident; then:
 //   warp 0      producer: one 2-D tensor copy of 128 rows x one step of packed weights per step
 //               into a 4-stage ring;
 //   warps 2, 3  issue the MMAs of alternate steps (one thread each); warp 2 owns tensor memory;
-//   warps 4-7   weight decoders: thread = row; packed word -> e4m3 bytes by a byte lookup
-//               (prmt) -> operand tiles (K-major core matrices, no swizzle);
-//   warps 8-11  drain: thread = row = accumulator lane; tcgen05.ld, scales, outputs.
+//   warps 4-11  weight decoders: thread = (row, half of the step); packed word -> e4m3 bytes by
+//               a byte lookup (prmt) -> operand tiles (K-major core matrices, no swizzle);
+//   warps 12-15 drain: thread = row = accumulator lane; tcgen05.ld, scales, outputs.
 // Four 128-column accumulators (8 blocks x 16 columns) let the MMAs run ahead of the drain.
 // Every wait is bounded and reports through the device error word.
 #pragma once
@@ -30,7 +30,7 @@
 
 namespace lb {
 
-constexpr int kTgThreads = 384;
+constexpr int kTgThreads = 512;
 constexpr int kTgRows = 128;                    // rows per unit (accumulator lanes)
 constexpr int kTgBlocks = 8;                    // q8_0 blocks per step
 constexpr int kTgCols = kTgBlocks * 32;         // columns per step
@@ -148,10 +148,10 @@ __global__ void __launch_bounds__(kTgThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTgPStages; s++) {
             mbar_init(&pk_full[s], 1);
-            mbar_init(&pk_empty[s], 4);
+            mbar_init(&pk_empty[s], 8);
         }
         for (int s = 0; s < kTgAStages; s++) {
-            mbar_init(&a_full[s], 4);  // four decoder warps
+            mbar_init(&a_full[s], 8);  // eight decoder warps
             mbar_init(&a_empty[s], 1);
         }
         for (int b = 0; b < kTgAccBufs; b++) {
@@ -264,9 +264,10 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             mma_commit(&mma_done);
             wait_or_report_tg(&mma_done, 0, p.err);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- weight decoders: thread = row ----------------
-        const int r = threadIdx.x - 128;
+    } else if (warp >= 4 && warp < 12) {
+        // ---------------- weight decoders: thread = (row, half of the step's blocks) ----------------
+        const int r = (threadIdx.x - 128) & (kTgRows - 1);
+        const int hh = (threadIdx.x - 128) >> 7;  // warps 4-7: blocks 0-3, warps 8-11: blocks 4-7
         int pi = 0, ai = 0;
         uint32_t pph = 0, aph = 0;
         bool ok = true;
@@ -287,7 +288,8 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             uint8_t *dst = wst + ai * kTgWStage + woff;
             if (F == kQ1) {
 #pragma unroll
-                for (int v = 0; v < kPB / 16; v++) {
+                for (int vv = 0; vv < kPB / 32; vv++) {
+                    const int v = hh * (kPB / 32) + vv;
                     const uint4 c = src[v ^ sw];
                     const uint32_t ws[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
@@ -301,7 +303,8 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                 }
             } else {
 #pragma unroll
-                for (int v = 0; v < kPB / 16; v++) {
+                for (int vv = 0; vv < kPB / 32; vv++) {
+                    const int v = hh * (kPB / 32) + vv;
                     const uint4 c = src[v ^ sw];  // Q2: blocks 2v, 2v+1; planar: one 64-column beat
                     uint4 c0, c1;
                     if (F == kQ2) {
@@ -336,11 +339,11 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                 aph ^= 1;
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 12) {
         // ---------------- drain: thread = row = accumulator lane ----------------
         // The step's scales are read from global memory (d_x: the same words for every lane;
         // d_w: the lane's row) before the accumulator wait.
-        const int r = threadIdx.x - 256;
+        const int r = threadIdx.x - 384;
         const int lq = warp & 3;
         int tb = 0;
         uint32_t tph = 0;
