@@ -18,7 +18,7 @@
 // 16 K bytes) is built once per CTA by warps 1-11 and stays resident; then:
 //   warp 0      producer: one 2-D tensor copy of 128 rows x one step of packed weights per step
 //               into a 4-stage ring;
-//   warps 2, 3  issue the MMAs of alternate steps (one thread each); warp 2 owns tensor memory;
+//   warps 1-3   issue the MMAs of every third step (one thread each); warp 2 owns tensor memory;
 //   warps 4-11  weight decoders: thread = (row, half of the step); packed word -> e4m3 bytes by
 //               a byte lookup (prmt) -> operand tiles (K-major core matrices, no swizzle);
 //   warps 12-15 drain: thread = row = accumulator lane; tcgen05.ld, scales, outputs.
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             mbar_init(&t_full[b], 1);
             mbar_init(&t_empty[b], 4);
         }
-        mbar_init(&mma_done, 2);
+        mbar_init(&mma_done, 3);
         fence_mbar_init();
     }
     // byte lookup: int8 code -> {e4m3(code >> 4), e4m3(code & 15)}
@@ -237,16 +237,16 @@ __global__ void __launch_bounds__(kTgThreads, 1)
         for (int i = max(0, issued - kTgPStages); i < issued; i++)
             mbar_wait(&pk_full[i % kTgPStages], (uint32_t)((i / kTgPStages) & 1));
 
-    } else if (warp == 2 || warp == 3) {
-        // ---------------- MMA issue: warp 2 + i issues the steps g = i (mod 2) ----------------
-        // (one thread each; issuer i owns accumulators i and i + 2)
+    } else if (warp >= 1 && warp <= 3) {
+        // ---------------- MMA issue: warp 1 + i issues the steps g = i (mod 3) ----------------
+        // (one thread each)
         if (lane == 0) {
             constexpr uint32_t idesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
             const int total = p.nunits <= (int)blockIdx.x
                                   ? 0
                                   : ((p.nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nsteps;
             const uint32_t wbase = smem_u32(wst), xbase = smem_u32(xop);
-            for (int g = warp - 2; g < total; g += 2) {
+            for (int g = warp - 1; g < total; g += 3) {
                 const int ai = g % kTgAStages, tb = g % kTgAccBufs;
                 if (!wait_or_report_tg(&a_full[ai], (uint32_t)((g / kTgAStages) & 1), p.err)) break;
                 if (!wait_or_report_tg(&t_empty[tb], (uint32_t)(((g / kTgAccBufs) & 1) ^ 1), p.err))
