@@ -60,7 +60,7 @@ struct TgMaps {
 template <int F>
 constexpr int tg_smem_bytes() {
     return kTgAStages * kTgWStage + kTgPStages * kTgRows * TgFmt<F>::kPitch +
-           (kTgMaxK / 32) * kTgXTile + 512 + 1024;
+           (kTgMaxK / 32) * kTgXTile + (kTgMaxK / 32) * 8 * 4 + 512 + 1024;
 }
 
 // Column permutation inside a 32-column block shared by the weight decode and the activation
@@ -137,7 +137,9 @@ __global__ void __launch_bounds__(kTgThreads, 1)
     uint8_t *wst = sm;                                            // weight operand stages
     uint8_t *pst = wst + kTgAStages * kTgWStage;                  // packed weight stages
     uint8_t *xop = pst + kTgPStages * kTgRows * kPP;              // activation operand, all K
-    uint16_t *lut = reinterpret_cast<uint16_t *>(xop + (kTgMaxK / 32) * kTgXTile);  // q -> e4m3 hi, lo
+    // activation scales d_x as binary32, [q8_0 block][token] (tokens past B unused)
+    float *dxf = reinterpret_cast<float *>(xop + (kTgMaxK / 32) * kTgXTile);
+    uint16_t *lut = reinterpret_cast<uint16_t *>(dxf + (kTgMaxK / 32) * 8);  // q -> e4m3 hi, lo
     __shared__ __align__(8) uint64_t pk_full[kTgPStages], pk_empty[kTgPStages], a_full[kTgAStages],
         a_empty[kTgAStages], t_full[kTgAccBufs], t_empty[kTgAccBufs], mma_done;
     __shared__ uint32_t tmem_slot;
@@ -197,6 +199,8 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                     lw[i] = prmt(e01, e23, 0x7531);
                 }
             }
+            if (F != kTrit && h == 0)
+                dxf[j * 8 + b] = b < B ? f16_bits_to_float(p.d[(int64_t)b * nq8 + j]) : 0.0f;
             uint8_t *tile = xop + j * kTgXTile;
             *reinterpret_cast<uint4 *>(tile + tg_off(b, 16 * h)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4 *>(tile + tg_off(8 + b, 16 * h)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -365,13 +369,9 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             }
             for (int s = 0; s < nsteps; s++) {
                 const int j0 = s * kTgBlocks;
-                // scales of the step (fp16), loaded before the wait
-                uint4 dxw[B];
+                // weight scales of the step (fp16), loaded before the wait
                 uint32_t dwp[F == kQ1 ? 1 : 2] = {};
                 if (F != kTrit) {
-#pragma unroll
-                    for (int b = 0; b < B; b++)
-                        dxw[b] = *reinterpret_cast<const uint4 *>(p.d + (int64_t)b * nq8 + j0);
                     if (F == kQ2) {
                         const uint2 v = *reinterpret_cast<const uint2 *>(M.scales + row * p.S + j0 / 2);
                         dwp[0] = v.x;
@@ -398,19 +398,22 @@ __global__ void __launch_bounds__(kTgThreads, 1)
 #pragma unroll
                     for (int t = 0; t < 2; t++) {
                         const int jb = 2 * pb + t;
+                        float dx[8];
+                        if (F != kTrit) {
+                            const float4 d0 = *reinterpret_cast<const float4 *>(dxf + (j0 + jb) * 8);
+                            const float4 d1 = *reinterpret_cast<const float4 *>(dxf + (j0 + jb) * 8 + 4);
+                            dx[0] = d0.x; dx[1] = d0.y; dx[2] = d0.z; dx[3] = d0.w;
+                            dx[4] = d1.x; dx[5] = d1.y; dx[6] = d1.z; dx[7] = d1.w;
+                        }
 #pragma unroll
                         for (int b = 0; b < B; b++) {
                             // isum = 16 S_hi + S_lo, exact
                             const float is = fmaf(16.0f, __uint_as_float(v[16 * t + b]),
                                                   __uint_as_float(v[16 * t + 8 + b]));
-                            if (F == kTrit) {
+                            if (F == kTrit)
                                 acc[b] += (Acc)(int)is;
-                            } else {
-                                const uint32_t dww = jb < 4 ? (jb < 2 ? dxw[b].x : dxw[b].y)
-                                                            : (jb < 6 ? dxw[b].z : dxw[b].w);
-                                const float dx = f16_bits_to_float((uint16_t)((jb & 1) ? (dww >> 16) : dww));
-                                tq[b] = fmaf(dx, is, tq[b]);
-                            }
+                            else
+                                tq[b] = fmaf(dx[b], is, tq[b]);
                         }
                         if (F != kTrit && (jb % kBlkPerW) == kBlkPerW - 1) {
                             const int wb = jb / kBlkPerW;  // weight block within the step
