@@ -753,12 +753,21 @@ inline int launch_stream(StreamParams &p, bool aux, int sms, cudaStream_t st) {
 template <int F, int B>
 inline int launch_tc_gemv(StreamParams &p, int sms, cudaStream_t st);
 
+// Fewest 128-row units for which the tensor-core variant beats the lane-per-row kernel: one of
+// its CTAs walks a unit's K in dependent steps of ~0.6 us, so a call with few units is latency-
+// bound there (measured at 8 tokens: 32 units 16.7 us vs 9.3 us lane-per-row, 108 units 11.7 vs
+// 15.4 us, 128 units 1107 vs 1058 GB/s).
+constexpr int64_t kTcMinUnits = 64;
+
 template <int F>
 inline int dispatch_stream(StreamParams &p, int B, bool aux, int sms, cudaStream_t st) {
     // Three or more tokens: the tensor-core variant (lb_tcgemv.cuh) when K is a multiple of
-    // its 256-column step and its activation operand (16 K bytes) fits in shared memory; the
-    // block-sum hook stays on the streaming kernels.
-    if (B >= 3 && !aux && p.K % 256 == 0 && p.K <= 4096) {
+    // its 256-column step, its activation operand (16 K bytes) fits in shared memory and the
+    // call has at least kTcMinUnits row units; the block-sum hook stays on the streaming
+    // kernels.
+    int64_t tc_units = 0;
+    for (int i = 0; i < p.G; i++) tc_units += (p.m[i].N + 127) / 128;
+    if (B >= 3 && !aux && p.K % 256 == 0 && p.K <= 4096 && tc_units >= kTcMinUnits) {
         switch (B) {
             case 3: return launch_tc_gemv<F, 3>(p, sms, st);
             case 4: return launch_tc_gemv<F, 4>(p, sms, st);

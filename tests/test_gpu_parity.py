@@ -361,6 +361,69 @@ def test_q_batched_ragged_production(qk, B):
         assert within(y, ref.y_exact, ref.mag)[0]
 
 
+def _tc_group_rows():
+    """Rows of a grouped call large enough (>= 64 units of 128 rows) for the tensor-core kernel:
+    31 ragged matrices of 130 rows, one of 77 and one of a single row (65 units)."""
+    return [130] * 31 + [77, 1]
+
+
+def _q_group(qk, Ns, K, B, seed):
+    blocks = (synth.q1_0_blocks(sum(Ns), K, seed=seed) if qk == 128 else
+              synth.q2_0_blocks(sum(Ns), K, seed=seed, probs=(0.25, 0.25, 0.25, 0.25)))
+    q, dx = _q8(B, K, seed=seed + 1)
+    bits, scales = repack_on_gpu(blocks, K, qk)
+    per_bits, per_sc = K // qk * 16, lb.scale_stride(K, qk)
+    mats, outs, r0 = [], [], 0
+    for n in Ns:
+        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
+        mats.append((bits[r0 * per_bits:(r0 + n) * per_bits], scales[r0 * per_sc:(r0 + n) * per_sc],
+                     y, None, n))
+        outs.append((blocks[r0:r0 + n], y))
+        r0 += n
+    fn = lb.lb_gemv_q1_0_grouped if qk == 128 else lb.lb_gemv_q2_0_g64_grouped
+    fn(mats, dev(q), dev(dx), K, B)
+    torch.cuda.synchronize()
+    return q, dx, outs
+
+
+@pytest.mark.parametrize("qk", [128, 64])
+@pytest.mark.parametrize("B", [3, 5, 8])
+@pytest.mark.parametrize("K", [1024, 4096])
+def test_q_batched_tensor_core(qk, B, K):
+    """Batch 3..8 on the tensor-core kernel (grouped call with >= 64 row units, K a multiple of
+    256 up to the resident maximum 4096): every matrix, ragged ones and a single row included,
+    within the GEMV bound of the oracle."""
+    q, dx, outs = _q_group(qk, _tc_group_rows(), K, B, seed=640 + B + K)
+    prod = oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product
+    for blocks, y in outs:
+        ref = prod(blocks, q, dx, want_isum=False)
+        ok, worst = within(host(y), ref.y_exact, ref.mag)
+        assert ok, worst
+
+
+@pytest.mark.parametrize("B", [3, 8])
+def test_trit_batched_tensor_core(B):
+    """Planar at batch 3..8 on the tensor-core kernel: bit-exact accumulators and outputs for
+    every matrix of a grouped call with >= 64 row units."""
+    Ns, K = _tc_group_rows(), 2560
+    planes, _ = synth.trit_planes(sum(Ns), K, seed=660 + B)
+    x = synth.activations(B, K, seed=670 + B)
+    qi, xs = oracle.quantize_i8_absmax(x)
+    mats, outs, r0 = [], [], 0
+    for n in Ns:
+        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
+        acc = torch.empty((B, n), dtype=torch.int32, device="cuda")
+        mats.append((dev(planes[r0:r0 + n]), 0.0173, y, acc, n))
+        outs.append((planes[r0:r0 + n], y, acc))
+        r0 += n
+    lb.lb_gemv_trit_planes_grouped(mats, dev(qi), dev(xs), K, B)
+    torch.cuda.synchronize()
+    for pl, y, acc in outs:
+        acc_ref, y_ref = oracle.trit_planes_product(pl, 0.0173, qi, xs)
+        assert np.array_equal(host(acc), acc_ref)
+        assert np.array_equal(host(y).view(np.uint32), y_ref.view(np.uint32))
+
+
 @pytest.mark.parametrize("B", [3, 8])
 def test_trit_batched_ragged(B):
     """Planar at batch 3..8 (lane-per-row kernel): bit-exact accumulators and outputs, ragged
