@@ -43,7 +43,23 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__rest
     }
 }
 
-// Per-token absmax int8: one CTA per token.
+// Per-token absmax int8: one CTA per token.  The first kHold float4 of each thread stay in
+// registers between the absmax pass and the quantize pass (one read of the row up to
+// K = 512 * 4 * kHold); the rest of a longer row is read twice.
+constexpr int kHold = 4;
+
+__device__ __forceinline__ uint32_t quantize_i8_word(float4 v, float s) {
+    const int c[4] = {__float2int_rn(__fmul_rn(v.x, s)), __float2int_rn(__fmul_rn(v.y, s)),
+                      __float2int_rn(__fmul_rn(v.z, s)), __float2int_rn(__fmul_rn(v.w, s))};
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int t = c[j] > 127 ? 127 : (c[j] < -128 ? -128 : c[j]);
+        w |= (uint32_t)(t & 0xFF) << (8 * j);
+    }
+    return w;
+}
+
 __global__ void __launch_bounds__(512) quantize_i8_absmax_kernel(const float *__restrict__ x,
                                                                  int8_t *__restrict__ q,
                                                                  float *__restrict__ x_scale,
@@ -55,7 +71,15 @@ __global__ void __launch_bounds__(512) quantize_i8_absmax_kernel(const float *__
     const float4 *xb = reinterpret_cast<const float4 *>(x + b * K);
     const int64_t nq = K / 4;
     float a = 0.0f;
-    for (int64_t i = threadIdx.x; i < nq; i += blockDim.x) {
+    float4 held[kHold];
+#pragma unroll
+    for (int r = 0; r < kHold; r++) {
+        const int64_t i = threadIdx.x + (int64_t)r * blockDim.x;
+        held[r] = i < nq ? xb[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 v = held[r];
+        a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    for (int64_t i = threadIdx.x + (int64_t)kHold * blockDim.x; i < nq; i += blockDim.x) {
         float4 v = xb[i];
         a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
@@ -72,18 +96,13 @@ __global__ void __launch_bounds__(512) quantize_i8_absmax_kernel(const float *__
     const float s = (amax != 0.0f) ? __fdiv_rn(127.0f, amax) : 0.0f;
     if (threadIdx.x == 0) x_scale[b] = __fdiv_rn(amax, 127.0f);
     uint32_t *qb = reinterpret_cast<uint32_t *>(q + b * K);
-    for (int64_t i = threadIdx.x; i < nq; i += blockDim.x) {
-        float4 v = xb[i];
-        int c[4] = {__float2int_rn(__fmul_rn(v.x, s)), __float2int_rn(__fmul_rn(v.y, s)),
-                    __float2int_rn(__fmul_rn(v.z, s)), __float2int_rn(__fmul_rn(v.w, s))};
-        uint32_t w = 0;
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            int t = c[j] > 127 ? 127 : (c[j] < -128 ? -128 : c[j]);
-            w |= (uint32_t)(t & 0xFF) << (8 * j);
-        }
-        qb[i] = w;
+    for (int r = 0; r < kHold; r++) {
+        const int64_t i = threadIdx.x + (int64_t)r * blockDim.x;
+        if (i < nq) qb[i] = quantize_i8_word(held[r], s);
     }
+    for (int64_t i = threadIdx.x + (int64_t)kHold * blockDim.x; i < nq; i += blockDim.x)
+        qb[i] = quantize_i8_word(xb[i], s);
 }
 
 // One thread per scale slot (n, j), j < S: block j of row n when j < nblk (fp16 scale to
