@@ -493,15 +493,19 @@ inline int launch_stream_cfg(StreamParams &p, const StreamPlan &pl, int sms, cud
 // once.  A unit is 32 rows; the eight consumer warps split its chunks and add their partial sums
 // through shared memory at the end of the unit.  Rows are staged one bulk copy per row (one per
 // producer lane) with a 16-byte pad, so the lanes' 16-byte weight reads do not conflict.
+// Calls with few rows use RG = 2 or 4 row groups per warp: a unit is then 32 / RG rows, lane
+// (row r, group g) takes every RG-th chunk of the warp's range starting at g, and the groups'
+// partial sums meet by warp shuffles -- RG times as many units, so small matrices fill the GPU.
+// The RG groups read RG consecutive chunks of the activation image at once (distinct banks).
 // ------------------------------------------------------------------------------------------
 constexpr int kRowsPerUnit = 32;
 
-template <int F, int B>
+template <int F, int B, int RG>
 __global__ void __launch_bounds__(kStreamThreads, 2)
     stream_rows_kernel(const __grid_constant__ StreamParams p) {
     constexpr int kCols = FmtInfo<F>::kCols;
     constexpr int kPer = kCols / 32;
-    constexpr int TR = kRowsPerUnit;
+    constexpr int TR = kRowsPerUnit / RG;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kMaxStages;
@@ -600,13 +604,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 return;
             }
             const uint8_t *sb = stages + (size_t)stage * p.stage_bytes;
-            const uint8_t *wrow = sb + (size_t)lane * wpitch;
+            const int lr = lane % TR, lg = lane / TR;  // row of the unit, chunk group
+            const uint8_t *wrow = sb + (size_t)lr * wpitch;
             const uint16_t *srow =
-                reinterpret_cast<const uint16_t *>(sb + (size_t)TR * wpitch + (size_t)lane * spitch);
+                reinterpret_cast<const uint16_t *>(sb + (size_t)TR * wpitch + (size_t)lr * spitch);
             // this warp's chunks of the stage: a contiguous eighth (rounded up)
             const int per = (kc + kConsumerWarps - 1) / kConsumerWarps;
             const int cb = warp * per, ce = min(kc, cb + per);
-            for (int c = cb; c < ce; c++) {
+            for (int c = cb + lg; c < ce; c += RG) {
                 const int cg = c0 + c;
                 const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + (size_t)c * 16);
                 const float dw = F != kTrit ? f16_bits_to_float(srow[c]) : 0.0f;
@@ -649,11 +654,17 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 phase ^= 1;
             }
         }
-        // add the eight warps' partial sums of this unit's rows
+        // add the row groups' partial sums (shuffles), then the eight warps' (shared memory)
 #pragma unroll
-        for (int b = 0; b < B; b++)
-            red[(warp * B + b) * TR + lane] = F == kTrit ? __int_as_float((int)acc[b])
-                                                         : (float)acc[b];
+        for (int o = TR; o < 32; o <<= 1)
+#pragma unroll
+            for (int b = 0; b < B; b++) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], o);
+        if (lane < TR) {
+#pragma unroll
+            for (int b = 0; b < B; b++)
+                red[(warp * B + b) * TR + lane] = F == kTrit ? __int_as_float((int)acc[b])
+                                                             : (float)acc[b];
+        }
         named_sync(1, kConsumerThreads);
         for (int i = threadIdx.x; i < B * TR; i += kConsumerThreads) {
             const int b = i / TR, r = i % TR;
@@ -679,26 +690,24 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     }
 }
 
-// Geometry of the batched variant: chunks per stage (whole row, or a multiple of 8 within a
-// 40 KB stage), stage count for two CTAs per SM where possible.
-inline StreamPlan plan_rows(int F, int B, int64_t K) {
+// Geometry of the batched variant for units of `tr` rows: chunks per stage (whole row, or a
+// multiple of 8 within a 40 KB stage), stage count for two CTAs per SM where possible.
+inline StreamPlan plan_rows(int F, int B, int64_t K, int tr) {
     const int cols = F == kQ1 ? 128 : 64;
     const int nchunk = (int)(K / cols);
     const int scale_b = F == kTrit ? 0 : 2;
     StreamPlan pl{};
     pl.act_bytes = (int)(((int64_t)B * K + (F == kTrit ? 0 : (int64_t)B * (K / 32) * 8) + 127) /
                          128 * 128);
-    auto stage_cost = [&](int kc) {
-        return kRowsPerUnit * ((kc + 1) * 16 + ((kc + 7) & ~7) * scale_b);
-    };
-    const int red_b = kConsumerWarps * B * kRowsPerUnit * 4;
+    auto stage_cost = [&](int kc) { return tr * ((kc + 1) * 16 + ((kc + 7) & ~7) * scale_b); };
+    const int red_b = kConsumerWarps * B * tr * 4;
     // Stage budget: two stages next to the activation image should still let two CTAs share
     // an SM (up to 40 KB per stage, at least 8 KB).
     int budget = (113 * 1024 - kBarBytes - pl.act_bytes - red_b) / 2;
     if (budget < 8 * 1024) budget = 40 * 1024;  // one CTA per SM anyway: large stages
     if (budget > 40 * 1024) budget = 40 * 1024;
     int KC = nchunk;
-    if (stage_cost(KC) > budget) KC = (budget / kRowsPerUnit - 16) / (16 + scale_b) / 8 * 8;
+    if (stage_cost(KC) > budget) KC = (budget / tr - 16) / (16 + scale_b) / 8 * 8;
     pl.RW = 0;
     pl.KC = KC;
     pl.nct = (nchunk + KC - 1) / KC;
@@ -712,10 +721,11 @@ inline StreamPlan plan_rows(int F, int B, int64_t K) {
     return pl;
 }
 
-template <int F, int B>
-inline int launch_rows(StreamParams &p, int sms, cudaStream_t st) {
-    const StreamPlan pl = plan_rows(F, B, p.K);
-    auto kern = stream_rows_kernel<F, B>;
+template <int F, int B, int RG>
+inline int launch_rows_cfg(StreamParams &p, int sms, cudaStream_t st) {
+    constexpr int TR = kRowsPerUnit / RG;
+    const StreamPlan pl = plan_rows(F, B, p.K, TR);
+    auto kern = stream_rows_kernel<F, B, RG>;
     int bps = 0;
     if (int e = prepare_kernel(reinterpret_cast<const void *>(kern), kStreamThreads,
                                (size_t)pl.smem, &bps))
@@ -723,7 +733,7 @@ inline int launch_rows(StreamParams &p, int sms, cudaStream_t st) {
     int units = 0;
     for (int i = 0; i < p.G; i++) {
         p.m[i].unit0 = units;
-        units += (p.m[i].N + kRowsPerUnit - 1) / kRowsPerUnit;
+        units += (p.m[i].N + TR - 1) / TR;
     }
     p.nunits = units;
     p.nct = pl.nct;
@@ -735,6 +745,19 @@ inline int launch_rows(StreamParams &p, int sms, cudaStream_t st) {
     if (grid > units) grid = units;
     if (grid < 1) grid = 1;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kStreamThreads), (size_t)pl.smem, st, p);
+}
+
+// Row groups per warp: as many (1, 2 or 4) as keep the call's units within two CTAs per SM,
+// with an eighth of slack (measured, 8 tokens, 2560 x 6912 planar: 320 units of 8 rows on 304
+// CTA slots 10.8 us, 160 units of 16 rows 12.2 us, 80 units of 32 rows 17.2 us).
+template <int F, int B>
+inline int launch_rows(StreamParams &p, int sms, cudaStream_t st) {
+    int64_t units32 = 0;
+    for (int i = 0; i < p.G; i++) units32 += (p.m[i].N + kRowsPerUnit - 1) / kRowsPerUnit;
+    const int64_t slots = 2 * (int64_t)sms;
+    if (4 * units32 <= slots + slots / 8) return launch_rows_cfg<F, B, 4>(p, sms, st);
+    if (2 * units32 <= slots) return launch_rows_cfg<F, B, 2>(p, sms, st);
+    return launch_rows_cfg<F, B, 1>(p, sms, st);
 }
 
 template <int F, int B>

@@ -361,6 +361,35 @@ def test_q_batched_ragged_production(qk, B):
         assert within(y, ref.y_exact, ref.mag)[0]
 
 
+@pytest.mark.parametrize("qk", [128, 64])
+@pytest.mark.parametrize("N", [2500, 5000])
+def test_q_batched_row_groups(qk, N):
+    """Lane-per-row kernel with two row groups per warp (2500 rows: 79 units of 32) and with one
+    (5000 rows: 157 units); K is not a multiple of 256, so the tensor-core kernel is not taken.
+    The small-matrix tests above run it with four row groups."""
+    K, B = (384 if qk == 128 else 320), 5
+    blocks = synth.q1_0_blocks(N, K, seed=680) if qk == 128 else synth.q2_0_blocks(
+        N, K, seed=680, probs=(0.25, 0.25, 0.25, 0.25))
+    q, dx = _q8(B, K, seed=681)
+    ref = (oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product)(blocks, q, dx,
+                                                                          want_isum=False)
+    y, _ = gemv_q(qk, blocks, q, dx, want_isum=False)
+    ok, worst = within(y, ref.y_exact, ref.mag)
+    assert ok, worst
+
+
+def test_trit_batched_row_groups():
+    """Planar down-projection shape (K = 6912) with two row groups per warp: bit-exact."""
+    N, K, B = 2500, 6912, 8
+    planes, _ = synth.trit_planes(N, K, seed=690)
+    x = synth.activations(B, K, seed=691)
+    qi, xs = oracle.quantize_i8_absmax(x)
+    acc_ref, y_ref = oracle.trit_planes_product(planes, 0.0173, qi, xs)
+    acc, y = gemv_trit(planes, 0.0173, qi, xs)
+    assert np.array_equal(acc, acc_ref)
+    assert np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
+
+
 def _tc_group_rows():
     """Rows of a grouped call large enough (>= 64 units of 128 rows) for the tensor-core kernel:
     31 ragged matrices of 130 rows, one of 77 and one of a single row (65 units)."""
