@@ -362,11 +362,11 @@ def test_q_batched_ragged_production(qk, B):
 
 
 @pytest.mark.parametrize("qk", [128, 64])
-@pytest.mark.parametrize("N", [2500, 5000])
+@pytest.mark.parametrize("N", [2500, 3500, 5000])
 def test_q_batched_row_groups(qk, N):
-    """Lane-per-row kernel with two row groups per warp (2500 rows: 79 units of 32) and with one
-    (5000 rows: 157 units); K is not a multiple of 256, so the tensor-core kernel is not taken.
-    The small-matrix tests above run it with four row groups."""
+    """Lane-per-row kernel with four row groups per warp (2500 rows: 79 units of 32), two (3500
+    rows: 110 units) and one (5000 rows: 157 units); K is not a multiple of 256, so the
+    tensor-core kernel is not taken."""
     K, B = (384 if qk == 128 else 320), 5
     blocks = synth.q1_0_blocks(N, K, seed=680) if qk == 128 else synth.q2_0_blocks(
         N, K, seed=680, probs=(0.25, 0.25, 0.25, 0.25))
@@ -378,9 +378,10 @@ def test_q_batched_row_groups(qk, N):
     assert ok, worst
 
 
-def test_trit_batched_row_groups():
-    """Planar down-projection shape (K = 6912) with two row groups per warp: bit-exact."""
-    N, K, B = 2500, 6912, 8
+@pytest.mark.parametrize("N", [2500, 3500])
+def test_trit_batched_row_groups(N):
+    """Planar down-projection shape (K = 6912) with four and two row groups per warp: bit-exact."""
+    K, B = 6912, 8
     planes, _ = synth.trit_planes(N, K, seed=690)
     x = synth.activations(B, K, seed=691)
     qi, xs = oracle.quantize_i8_absmax(x)
