@@ -4,7 +4,8 @@
 // the largest single weight stream of a token; it is stored bf16 (the checkpoint's precision)
 // and widened exactly for an f32 product.  Widening bf16 is a 16-bit left shift.
 //
-// GPU design: each lane streams 16-byte chunks (8 weights) of R rows with L1-bypassing loads;
+// GPU design: each lane streams 16-byte chunks (8 weights) of R rows (8 at one or two tokens,
+// 4 otherwise: every activation read from shared memory serves R rows) with L1-bypassing loads;
 // the B activation rows sit in shared memory (fp32, swizzled per 16 bytes so 8 consecutive
 // lanes read distinct banks) and are reused for the R rows; fp32 FMAs accumulate per lane, and a
 // warp-shuffle tree finishes each row.
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(kBfThreads)
 template <int B>
 static int launch_bf16(const uint16_t *w, const float *x, float *y, int64_t N, int64_t K,
                        int sms, cudaStream_t st) {
-    constexpr int R = B <= 2 ? 4 : (B <= 4 ? 2 : 1);
+    constexpr int R = B <= 2 ? 8 : 4;
     const size_t smem = (size_t)B * K * 4;
     auto kern = gemv_bf16_kernel<B, R>;
     int bps = 0;

@@ -241,7 +241,7 @@ def test_trit_minus128_extremes():
 # ----------------------------------------------------------------------------------------------
 # bf16 head
 # ----------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("B", [1, 2, 4, 8])
+@pytest.mark.parametrize("B", [1, 2, 3, 4, 8])
 def test_bf16_ragged(B):
     N, K = 37, 328 if B % 2 else 2568
     w = synth.bf16_weights(N, K, seed=800 + B)
