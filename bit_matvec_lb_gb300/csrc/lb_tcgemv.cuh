@@ -256,12 +256,16 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                 if (!wait_or_report_tg(&t_empty[tb], (uint32_t)(((g / kTgAccBufs) & 1) ^ 1), p.err))
                     break;
                 tc_fence_after();
+                // descriptors of the step's first block; the others follow by adding the tile
+                // offsets to the start-address field (smem addresses stay below 2^18, so the
+                // 14-bit field of addr >> 4 cannot carry into the next field)
+                const uint64_t ad0 = smem_desc8(wbase + ai * kTgWStage);
+                const uint64_t bd0 = smem_desc8(xbase + (g % nsteps) * kTgBlocks * kTgXTile);
+                const uint32_t d0 = tmem + (uint32_t)(tb * 128);
 #pragma unroll
-                for (int jb = 0; jb < kTgBlocks; jb++) {
-                    const uint64_t ad = smem_desc8(wbase + ai * kTgWStage + jb * kTgWTile);
-                    const uint64_t bd = smem_desc8(xbase + ((g % nsteps) * kTgBlocks + jb) * kTgXTile);
-                    mma_f8(tmem + (uint32_t)(tb * 128 + jb * 16), ad, bd, idesc);
-                }
+                for (int jb = 0; jb < kTgBlocks; jb++)
+                    mma_f8(d0 + (uint32_t)(jb * 16), ad0 + (uint64_t)((jb * kTgWTile) >> 4),
+                           bd0 + (uint64_t)((jb * kTgXTile) >> 4), idesc);
                 mma_commit(&a_empty[ai]);
                 mma_commit(&t_full[tb]);
             }
