@@ -538,18 +538,22 @@ def rows_prefill(lb, rows, stream):
     ds = {k: torch.empty((M, k // 32), dtype=torch.int16, device="cuda") for k in (4096, 12288)}
     ws = torch.empty(lb.lb_gemm_workspace_bytes(M, 12288), dtype=torch.uint8, device="cuda")
     ops = 2 * M * sum(n * k for _, n, k in synth.QWEN3_8B_PROJ)
+    # q|k|v and gate|up read the same activation: one grouped GEMM each
+    groups = [(0, 1, 2), (3,), (4, 5), (6,)]
     for fmt in ("q2_0_g64", "q1_0"):
         make = make_q2_weights if fmt == "q2_0_g64" else make_q1_weights
-        gemm = lb.lb_gemm_q2_0_g64 if fmt == "q2_0_g64" else lb.lb_gemm_q1_0
+        gemm = lb.lb_gemm_q2_0_g64_grouped if fmt == "q2_0_g64" else lb.lb_gemm_q1_0_grouped
         proj = [(make(n, k, synth.proj_seed(90_000, 0, i)), n, k)
                 for i, (_, n, k) in enumerate(synth.QWEN3_8B_PROJ)]
         ys = [torch.empty((M, n), dtype=torch.float32, device="cuda") for _, n, _ in proj]
 
         def layer():
-            for i, ((wb, sc), n, k) in enumerate(proj):
-                if i in (0, 3, 4, 6):  # attention input, attention output, FFN input, FFN mid
-                    lb.lb_quantize_q8_0(xs[k], qs[k], ds[k], M, k, stream=stream)
-                gemm(wb, sc, qs[k], ds[k], ys[i], M, n, k, ws, stream=stream)
+            # one q8_0 per group: attention input, attention output, FFN input, FFN mid
+            for members in groups:
+                k = proj[members[0]][2]
+                lb.lb_quantize_q8_0(xs[k], qs[k], ds[k], M, k, stream=stream)
+                gemm([(proj[i][0][0], proj[i][0][1], ys[i], proj[i][1]) for i in members],
+                     qs[k], ds[k], M, k, ws, stream=stream)
         ms = time_graph(Graph(layer, stream), reps=20)
         tops = ops / (ms * 1e-3) / 1e12
         rows[f"qwen3_8b_prefill_m512_{fmt}"] = {

@@ -52,6 +52,13 @@ class lb_trit_matrix(ctypes.Structure):
     _fields_ = [("planes", P), ("w_scale", F32), ("y", P), ("acc_opt", P), ("N", I64)]
 
 
+class lb_gemm_matrix(ctypes.Structure):
+    _fields_ = [("bits", P), ("scales", P), ("y", P), ("N", I64)]
+
+
+GEMM_MAX_GROUP = 8
+
+
 SIGNATURES = {
     "lb_status_string": (ctypes.c_char_p, [I32]),
     "lb_version": (I32, []),
@@ -74,6 +81,10 @@ SIGNATURES = {
     "lb_gemm_q1_0": (I32, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
     "lb_gemm_q2_0_g64": (I32, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
     "lb_gemm_q2_0_g64_noalloc": (I32, [P, P, P, P, P, I64, I64, I64, P]),
+    "lb_gemm_q1_0_grouped": (I32, [ctypes.POINTER(lb_gemm_matrix), I32, P, P, I64, I64, P,
+                                   ctypes.c_size_t, P]),
+    "lb_gemm_q2_0_g64_grouped": (I32, [ctypes.POINTER(lb_gemm_matrix), I32, P, P, I64, I64, P,
+                                       ctypes.c_size_t, P]),
 }
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -259,6 +270,31 @@ def lb_gemm_q2_0_g64(codes, scales, q, d, y, M: int, N: int, K: int, workspace,
                      workspace_bytes=None, stream=None):
     _gemm("lb_gemm_q2_0_g64", codes, scales, q, d, y, M, N, K, workspace, workspace_bytes,
           stream)
+
+
+def _gemm_grouped(name, mats, q, d, M, K, workspace, workspace_bytes, stream):
+    if not 1 <= len(mats) <= GEMM_MAX_GROUP:
+        raise ValueError(f"a GEMM group holds 1..{GEMM_MAX_GROUP} matrices")
+    arr = (lb_gemm_matrix * len(mats))()
+    for i, (bits, scales, y, N) in enumerate(mats):
+        arr[i] = lb_gemm_matrix(_ptr(bits), _ptr(scales), _ptr(y), int(N))
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(name, getattr(load(), name)(arr, len(mats), _ptr(q), _ptr(d), int(M), int(K),
+                                       _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def lb_gemm_q1_0_grouped(mats, q, d, M: int, K: int, workspace, workspace_bytes=None,
+                         stream=None):
+    """mats: sequence of (bits, scales, y, N) sharing the activation q, d (one launch)."""
+    _gemm_grouped("lb_gemm_q1_0_grouped", mats, q, d, M, K, workspace, workspace_bytes, stream)
+
+
+def lb_gemm_q2_0_g64_grouped(mats, q, d, M: int, K: int, workspace, workspace_bytes=None,
+                             stream=None):
+    """mats: sequence of (codes, scales, y, N) sharing the activation q, d (one launch)."""
+    _gemm_grouped("lb_gemm_q2_0_g64_grouped", mats, q, d, M, K, workspace, workspace_bytes,
+                  stream)
 
 
 def lb_gemm_q2_0_g64_noalloc(codes, scales, q, d, y, M: int, N: int, K: int, stream=None):

@@ -48,14 +48,21 @@ constexpr int kGemmSmem = kTotOffset + kTotBytes + 1024;
 
 enum GFmt { kG1 = 0, kG2 = 1 };
 
-struct GemmParams {
+// One weight matrix of a (possibly grouped) call: the call's tiles are those of matrix 0, then
+// of matrix 1, ...; tile0 is the index of the matrix's first tile.
+struct GemmMat {
     const uint8_t *bits;     // [N][K/8] (Q1_0) or [N][K/4] (Q2_0_g64)
     const uint16_t *scales;  // [N][S]
+    float *y;                // [M][N]
+    int N, tile0;
+};
+
+struct GemmParams {
+    GemmMat mat[LB_GEMM_MAX_GROUP];
     const uint8_t *ws;       // activation tiles [mtiles][K/32][8192 B]
     const uint16_t *d;       // [M][K/32] q8_0 scales
-    float *y;                // [M][N]
     int *err;
-    int M, N, K, S, nK32, mtiles;
+    int G, M, K, S, nK32, mtiles;
 };
 
 // ------------------------------------------------------------------------------------------
@@ -183,8 +190,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tempty[kAccBufs], mma_done;
     __shared__ uint32_t tmem_slot;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m_tile = blockIdx.x % p.mtiles;
-    const int n_tile = blockIdx.x / p.mtiles;
+    int gi = 0;
+    while (gi + 1 < p.G && p.mat[gi + 1].tile0 <= (int)blockIdx.x) gi++;
+    const GemmMat &W = p.mat[gi];
+    const int m_tile = ((int)blockIdx.x - W.tile0) % p.mtiles;
+    const int n_tile = ((int)blockIdx.x - W.tile0) / p.mtiles;
     const int64_t m0 = (int64_t)m_tile * kTileM, n0 = (int64_t)n_tile * kTileN;
     const int nK32 = p.nK32;       // even: K is a multiple of 64
     const int nst = nK32 / 2;      // stages of two K32 steps
@@ -212,11 +222,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
         constexpr int kQ = 4;
         const int nl = threadIdx.x;
         const int64_t n = n0 + nl;
-        const bool valid = n < p.N;
+        const bool valid = n < W.N;
         const int64_t nn = valid ? n : 0;
         constexpr int kStBytes = F == kG2 ? 16 : 8;       // packed bytes per stage and row
-        const uint8_t *row = p.bits + nn * (int64_t)nst * kStBytes;
-        const uint16_t *srow = p.scales + nn * (int64_t)p.S;
+        const uint8_t *row = W.bits + nn * (int64_t)nst * kStBytes;
+        const uint16_t *srow = W.scales + nn * (int64_t)p.S;
         // Q2_0_g64: a stage is one 64-weight block (16 code bytes, one scale); Q1_0: half of a
         // 128-weight block (8 sign bytes; the scale of block st / 2).
         auto load_stage = [&](int st, uint4 &c, uint32_t &sc) {
@@ -398,11 +408,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
             const int ml = wd * (kTileM / 8) + rr;
             const int64_t mm = m0 + ml;
             if (mm >= p.M) break;
-            float *yrow = p.y + mm * (int64_t)p.N;
+            float *yrow = W.y + mm * (int64_t)W.N;
 #pragma unroll
             for (int i = 0; i < kTileN / 32; i++) {
                 const int nl = i * 32 + lane;
-                if (n0 + nl < p.N) yrow[n0 + nl] = tot[nl * kTotPitch + ml];
+                if (n0 + nl < W.N) yrow[n0 + nl] = tot[nl * kTotPitch + ml];
             }
         }
     }
@@ -414,21 +424,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
     }
 }
 
-static int gemm_q(int F, const uint8_t *bits, const uint16_t *scales, const int8_t *q,
-                  const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K, void *workspace,
-                  size_t workspace_bytes, void *stream) {
+// Checks and launches of a call over G weight matrices sharing one activation (G = 1 for the
+// single-matrix entry points): one prologue for the activation, one launch for every tile of
+// every matrix.
+static int gemm_q_group(int F, const lb_gemm_matrix *mats, int G, const int8_t *q,
+                        const uint16_t *d, int64_t M, int64_t K, void *workspace,
+                        size_t workspace_bytes, void *stream) {
     const int qk = F == kG1 ? 128 : 64;
-    if (!bits || !scales || !q || !d || !y || !workspace) return LB_ERR_NULL;
-    if (!aligned16(bits) || !aligned16(scales) || !aligned16(q) || !aligned16(d) ||
-        !aligned16(y) || !aligned16(workspace))
-        return LB_ERR_ALIGN;
-    if (M < 1 || N < 1 || K < qk || K % qk != 0 || M > (1 << 30) || N > (1 << 30) ||
-        K > (1 << 24))
-        return LB_ERR_SHAPE;
+    if (!mats || !q || !d || !workspace) return LB_ERR_NULL;
+    if (G < 1 || G > LB_GEMM_MAX_GROUP) return LB_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(d) || !aligned16(workspace)) return LB_ERR_ALIGN;
+    if (M < 1 || K < qk || K % qk != 0 || M > (1 << 30) || K > (1 << 24)) return LB_ERR_SHAPE;
     const int64_t mtiles = (M + kTileM - 1) / kTileM;
-    const int64_t ntiles = (N + kTileN - 1) / kTileN;
     if (workspace_bytes < (size_t)(mtiles * kTileM * K * 2)) return LB_ERR_SHAPE;
-    if (mtiles * ntiles > 0x7fffffff) return LB_ERR_SHAPE;
+    GemmParams p{};
+    int64_t tiles = 0;
+    for (int i = 0; i < G; i++) {
+        const lb_gemm_matrix &m = mats[i];
+        if (!m.bits || !m.scales || !m.y) return LB_ERR_NULL;
+        if (!aligned16(m.bits) || !aligned16(m.scales) || !aligned16(m.y)) return LB_ERR_ALIGN;
+        if (m.N < 1 || m.N > (1 << 30)) return LB_ERR_SHAPE;
+        p.mat[i].bits = m.bits;
+        p.mat[i].scales = m.scales;
+        p.mat[i].y = m.y;
+        p.mat[i].N = (int)m.N;
+        p.mat[i].tile0 = (int)tiles;
+        tiles += mtiles * ((m.N + kTileN - 1) / kTileN);
+        if (tiles > 0x7fffffff) return LB_ERR_SHAPE;
+    }
     DeviceInfo di;
     if (int st = current_device_info(&di)) return st;
     cudaStream_t st = as_stream(stream);
@@ -441,15 +464,11 @@ static int gemm_q(int F, const uint8_t *bits, const uint16_t *scales, const int8
                      : launch_pdl(gemm_prep_act_kernel<kG2>, dim3((unsigned)pgrid), dim3(256), 0,
                                   st, q, (uint8_t *)workspace, (int)M, (int)K, (int)mtiles);
     if (e) return e;
-    GemmParams p{};
-    p.bits = bits;
-    p.scales = scales;
     p.ws = (const uint8_t *)workspace;
     p.d = d;
-    p.y = y;
     p.err = device_error_word();
+    p.G = G;
     p.M = (int)M;
-    p.N = (int)N;
     p.K = (int)K;
     p.S = (int)((K / qk + 7) / 8 * 8);
     p.nK32 = (int)(K / 32);
@@ -459,8 +478,14 @@ static int gemm_q(int F, const uint8_t *bits, const uint16_t *scales, const int8
     if (int e2 = prepare_kernel(reinterpret_cast<const void *>(kern), kGemmThreads, kGemmSmem,
                                 &bps))
         return e2;
-    return launch_pdl(kern, dim3((unsigned)(mtiles * ntiles)), dim3(kGemmThreads), kGemmSmem, st,
-                      p);
+    return launch_pdl(kern, dim3((unsigned)tiles), dim3(kGemmThreads), kGemmSmem, st, p);
+}
+
+static int gemm_q(int F, const uint8_t *bits, const uint16_t *scales, const int8_t *q,
+                  const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K, void *workspace,
+                  size_t workspace_bytes, void *stream) {
+    const lb_gemm_matrix m = {bits, scales, y, N};
+    return gemm_q_group(F, &m, 1, q, d, M, K, workspace, workspace_bytes, stream);
 }
 
 }  // namespace lb
@@ -482,6 +507,18 @@ LB_EXPORT int lb_gemm_q2_0_g64(const uint8_t *codes, const uint16_t *scales, con
                                const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K,
                                void *workspace, size_t workspace_bytes, void *stream) {
     return gemm_q(kG2, codes, scales, q, d, y, M, N, K, workspace, workspace_bytes, stream);
+}
+
+LB_EXPORT int lb_gemm_q1_0_grouped(const lb_gemm_matrix *mats, int G, const int8_t *q,
+                                   const uint16_t *d, int64_t M, int64_t K, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+    return gemm_q_group(kG1, mats, G, q, d, M, K, workspace, workspace_bytes, stream);
+}
+
+LB_EXPORT int lb_gemm_q2_0_g64_grouped(const lb_gemm_matrix *mats, int G, const int8_t *q,
+                                       const uint16_t *d, int64_t M, int64_t K, void *workspace,
+                                       size_t workspace_bytes, void *stream) {
+    return gemm_q_group(kG2, mats, G, q, d, M, K, workspace, workspace_bytes, stream);
 }
 
 namespace lb {

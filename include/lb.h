@@ -226,6 +226,28 @@ int lb_gemm_q2_0_g64(const uint8_t *codes, const uint16_t *scales, const int8_t 
                      const uint16_t *d, float *y, int64_t M, int64_t N, int64_t K,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* Grouped prefill GEMM: mats[0..G-1] (host array, 1 <= G <= LB_GEMM_MAX_GROUP, read during
+ * the call) against ONE q8_0 activation q, d of M tokens and K columns, in one launch -- for
+ * example the q, k and v projections, or gate and up.  Same arithmetic, accuracy, workspace and
+ * errors as the single-matrix calls, whose results it reproduces bit for bit; each matrix has
+ * its own rows N, weights and output y [M][N].  Outputs must not overlap.  A convenience of this
+ * library (the pages run projections one at a time); it lets small matrices (k, v: N = 1024)
+ * share the GPU with the others instead of running alone. */
+#define LB_GEMM_MAX_GROUP 8
+typedef struct lb_gemm_matrix {
+    const uint8_t *bits;     /* repacked sign bytes (Q1_0) or code bytes (Q2_0_g64) */
+    const uint16_t *scales;  /* [N][LB_SCALE_STRIDE(K, QK)] fp16 */
+    float *y;                /* [M][N] fp32 output */
+    int64_t N;               /* rows, 1 <= N <= 2^30 */
+} lb_gemm_matrix;
+
+int lb_gemm_q1_0_grouped(const lb_gemm_matrix *mats, int G, const int8_t *q, const uint16_t *d,
+                         int64_t M, int64_t K, void *workspace, size_t workspace_bytes,
+                         void *stream);
+int lb_gemm_q2_0_g64_grouped(const lb_gemm_matrix *mats, int G, const int8_t *q,
+                             const uint16_t *d, int64_t M, int64_t K, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
 /* ---- Q2_0_g64 prefill GEMM without caller scratch.
  * No counterpart in the source pages: a convenience of this library for callers that cannot
  * allocate device memory.  Same arithmetic, accuracy, layouts and errors as lb_gemm_q2_0_g64,

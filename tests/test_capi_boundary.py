@@ -141,6 +141,30 @@ def test_grouped_refusals(lib):
     assert lib.lb_gemv_trit_planes_grouped(t, 1, A, A, 64, 9, None) == -4
 
 
+@pytest.mark.parametrize("fn,qk", [("lb_gemm_q1_0_grouped", 128), ("lb_gemm_q2_0_g64_grouped", 64)])
+def test_gemm_grouped_refusals(lib, fn, qk):
+    f = getattr(lib, fn)
+    K = 4 * qk
+    ws = lib.lb_gemm_workspace_bytes(16, K)
+    arr = (lb.lb_gemm_matrix * 9)()
+    for i in range(9):
+        arr[i] = lb.lb_gemm_matrix(A, A, A, 8)
+    assert f(arr, 0, A, A, 16, K, A, ws, None) == -3      # empty group
+    assert f(arr, 9, A, A, 16, K, A, ws, None) == -3      # more than LB_GEMM_MAX_GROUP
+    assert f(None, 2, A, A, 16, K, A, ws, None) == -1
+    assert f(arr, 2, None, A, 16, K, A, ws, None) == -1
+    assert f(arr, 2, A, A, 16, K, None, ws, None) == -1
+    assert f(arr, 2, MIS, A, 16, K, A, ws, None) == -2
+    assert f(arr, 2, A, A, 16, K + 32, A, ws, None) == -3
+    assert f(arr, 2, A, A, 16, K, A, ws - 1, None) == -3  # workspace one byte short
+    arr[1] = lb.lb_gemm_matrix(A, None, A, 8)
+    assert f(arr, 2, A, A, 16, K, A, ws, None) == -1      # NULL scales of matrix 1
+    arr[1] = lb.lb_gemm_matrix(A, A, MIS, 8)
+    assert f(arr, 2, A, A, 16, K, A, ws, None) == -2      # misaligned y of matrix 1
+    arr[1] = lb.lb_gemm_matrix(A, A, A, 0)
+    assert f(arr, 2, A, A, 16, K, A, ws, None) == -3      # N = 0
+
+
 def test_scale_stride():
     assert lb.scale_stride(512, 128) == 8 and lb.scale_stride(4096, 64) == 64
     assert lb.scale_stride(4224, 128) == 40 and lb.scale_stride(320, 64) == 8

@@ -155,5 +155,31 @@ def test_gemm_prefill_shapes_sampled(qk, name, N, K):
     assert ok, f"worst err/tol = {worst:.3g}"
 
 
+@pytest.mark.parametrize("qk", [128, 64])
+def test_gemm_grouped(qk):
+    """Grouped call: three ragged matrices (130, 1, 257 rows) sharing one activation of 130
+    tokens; every output within the bound of the oracle and bit-identical to the single-matrix
+    call on the same weights."""
+    M, K, Ns = 130, 1152 if qk == 128 else 1216, (130, 1, 257)
+    q, dx = oracle.quantize_q8_0(synth.activations(M, K, seed=940))
+    ws = torch.empty(lb.lb_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    mats, outs = [], []
+    for i, n in enumerate(Ns):
+        blocks = _blocks(qk, n, K, seed=950 + i)
+        bits, scales = repack_on_gpu(blocks, K, qk)
+        y = torch.full((M, n), float("nan"), dtype=torch.float32, device="cuda")
+        mats.append((bits, scales, y, n))
+        outs.append((blocks, bits, scales, y))
+    fn = lb.lb_gemm_q1_0_grouped if qk == 128 else lb.lb_gemm_q2_0_g64_grouped
+    fn(mats, dev(q), dev(dx), M, K, ws)
+    torch.cuda.synchronize()
+    for blocks, bits, scales, y in outs:
+        ref = _ref(qk, blocks, q, dx)
+        ok, worst = within(y.cpu().numpy(), ref.y_exact, ref.mag)
+        assert ok, worst
+        y1 = gemm_q(qk, blocks, q, dx, repacked=(bits, scales))
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), y1.view(np.uint32))
+
+
 def test_gemm_device_status_clean():
     assert lb.lb_device_status() == 0
