@@ -14,7 +14,7 @@
  *   [BH]  bankml BUILD_HISTORY.md, phase ledger item "P2 -- own the kernels".
  *   [TA]  tritium.technology "Architecture", sections 1, 2, 3, 4.1, 5, 8.
  *
- * Readings taken where the pages are silent (each is also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   R1  q8_0 reciprocal is 127/amax (as [TR] III.2 and [BH] state), not 1/d.
  *   R2  q8_0 rounding is round-half-to-even ([TR] III.2, [BH]).
  *   R3  Q1_0 sign polarity: bit 1 means +1, bit 0 means -1 (the all-bits-set block
