@@ -192,6 +192,31 @@ def test_qwen3_shapes_sampled(qk, name, N, K):
     assert within(y[:, rows], ref.y_exact, ref.mag)[0]
 
 
+@pytest.mark.parametrize("G", [1, 16])
+def test_q2_4096_batch8_sampled(G):
+    """The 4096 x 4096 Q2_0_g64 workload at 8 tokens as the bench runs it: one matrix (32 units:
+    the lane-per-row kernel with four row groups) and a group of 16 (512 units: the tensor-core
+    kernel); sampled rows of the first and last matrix checked against the oracle."""
+    N, K, B = 4096, 4096, 8
+    blocks = [synth.q2_0_blocks(N, K, seed=820 + i) for i in (0, G - 1)] if G > 1 else \
+        [synth.q2_0_blocks(N, K, seed=820)]
+    q, dx = _q8(B, K, seed=821)
+    reps = [repack_on_gpu(bl, K, 64) for bl in blocks]
+    mats, ys = [], []
+    for i in range(G):
+        bits, scales = reps[0] if i < G - 1 or G == 1 else reps[-1]
+        y = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
+        mats.append((bits, scales, y, None, N))
+        ys.append(y)
+    lb.lb_gemv_q2_0_g64_grouped(mats, dev(q), dev(dx), K, B)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(0, N, 41), [N - 1]]))
+    for bl, y in ((blocks[0], ys[0]), (blocks[-1], ys[-1])):
+        ref = oracle.q2_0_g64_product(bl[rows], q, dx, want_isum=False)
+        ok, worst = within(host(y)[:, rows], ref.y_exact, ref.mag)
+        assert ok, worst
+
+
 # ----------------------------------------------------------------------------------------------
 # planar ternary
 # ----------------------------------------------------------------------------------------------
