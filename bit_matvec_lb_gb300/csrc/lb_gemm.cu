@@ -242,41 +242,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
                 sc = srow[st >> 1];
             }
         };
+        // Slot j of the queue holds the stages j, j + kQ, j + 2 kQ, ...: the stage loop is unrolled
+        // by kQ so that every slot is a fixed register set, refilled right after its last use.
+        // (Shifting the queue by one slot per stage would make each shift wait for the load
+        // issued one stage earlier -- a full memory latency per stage.)
         uint4 qc[kQ];
         uint32_t qs[kQ];
 #pragma unroll
         for (int i = 0; i < kQ; i++) load_stage(i, qc[i], qs[i]);
         const uint32_t boff = (uint32_t)canon_offset(nl, 0) + 2 * kTileBytes;
         Ring<kStages> rs;
-        for (int st = 0; st < nst; st++) {
-            const uint4 cw = qc[0];
-            const uint32_t sc = qs[0];
+        bool ok = true;
+        for (int st0 = 0; st0 < nst && ok; st0 += kQ) {
 #pragma unroll
-            for (int i = 0; i + 1 < kQ; i++) {
-                qc[i] = qc[i + 1];
-                qs[i] = qs[i + 1];
-            }
-            load_stage(st + kQ, qc[kQ - 1], qs[kQ - 1]);
-            if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase ^ 1u))) {
-                if (lane == 0) atomicOr(p.err, 1);
-                break;
-            }
-            uint8_t *bt = gsm + rs.idx * kStageBytes + boff;
+            for (int j = 0; j < kQ; j++) {
+                const int st = st0 + j;
+                if (st >= nst) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase ^ 1u))) {
+                    if (lane == 0) atomicOr(p.err, 1);
+                    ok = false;
+                    break;
+                }
+                uint8_t *bt = gsm + rs.idx * kStageBytes + boff;
 #pragma unroll
-            for (int t = 0; t < 2; t++) {
-                uint4 c[4];
-                if (F == kG2)
-                    expand_q2(t ? cw.z : cw.x, t ? cw.w : cw.y, __ushort_as_half((uint16_t)sc), c);
-                else
-                    expand_q1(t ? cw.y : cw.x, (uint16_t)sc, c);
+                for (int t = 0; t < 2; t++) {
+                    uint4 c[4];
+                    if (F == kG2)
+                        expand_q2(t ? qc[j].z : qc[j].x, t ? qc[j].w : qc[j].y,
+                                  __ushort_as_half((uint16_t)qs[j]), c);
+                    else
+                        expand_q1(t ? qc[j].y : qc[j].x, (uint16_t)qs[j], c);
 #pragma unroll
-                for (int kc = 0; kc < 4; kc++)
-                    *reinterpret_cast<uint4 *>(bt + t * kTileBytes + kc * kCoreLBO) = c[kc];
+                    for (int kc = 0; kc < 4; kc++)
+                        *reinterpret_cast<uint4 *>(bt + t * kTileBytes + kc * kCoreLBO) = c[kc];
+                }
+                load_stage(st + kQ, qc[j], qs[j]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[rs.idx]);
+                rs.next();
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[rs.idx]);
-            rs.next();
         }
     } else if (warp == 4) {
         // ---------------- activation tiles: one 16 KB bulk copy per stage ----------------
