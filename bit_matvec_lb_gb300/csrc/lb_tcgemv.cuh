@@ -349,8 +349,8 @@ __global__ void __launch_bounds__(kTgThreads, 1)
         }
     } else if (warp >= 12) {
         // ---------------- drain: thread = row = accumulator lane ----------------
-        // The step's scales are read from global memory (d_x: the same words for every lane;
-        // d_w: the lane's row) before the accumulator wait.
+        // d_x comes from the shared table built in the prologue; d_w (the lane's row) from
+        // global memory, two steps ahead of its use.
         const int r = threadIdx.x - 384;
         const int lq = warp & 3;
         int tb = 0;
@@ -371,69 +371,78 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                 acc[b] = 0;
                 tq[b] = 0.0f;
             }
-            for (int s = 0; s < nsteps; s++) {
-                const int j0 = s * kTgBlocks;
-                // weight scales of the step (fp16), loaded before the wait
-                uint32_t dwp[F == kQ1 ? 1 : 2] = {};
-                if (F != kTrit) {
-                    if (F == kQ2) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(M.scales + row * p.S + j0 / 2);
-                        dwp[0] = v.x;
-                        dwp[1] = v.y;
-                    } else {
-                        dwp[0] = *reinterpret_cast<const uint32_t *>(M.scales + row * p.S + j0 / 4);
-                    }
+            // Weight scales two steps ahead in two fixed register slots (the loop is unrolled by
+            // two so that no register move waits for the newest load; they come from HBM).
+            auto dload = [&](int ss) {
+                uint2 v = make_uint2(0u, 0u);
+                if (F != kTrit && ss < nsteps) {
+                    if (F == kQ2)
+                        v = *reinterpret_cast<const uint2 *>(M.scales + row * p.S + ss * (kTgBlocks / 2));
+                    else
+                        v.x = *reinterpret_cast<const uint32_t *>(M.scales + row * p.S + ss * (kTgBlocks / 4));
                 }
-                if (!__all_sync(0xffffffffu, mbar_wait(&t_full[tb], tph))) {
-                    if (lane == 0) report(p.err);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                return v;
+            };
+            uint2 dslot[2] = {dload(0), dload(1)};
+            for (int s0 = 0; s0 < nsteps && ok; s0 += 2) {
 #pragma unroll
-                for (int pb = 0; pb < kTgBlocks / 2; pb++) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(tb * 128 + pb * 32), v);
-                    if (pb == kTgBlocks / 2 - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&t_empty[tb]);
+                for (int hs = 0; hs < 2; hs++) {
+                    const int s = s0 + hs;
+                    if (s >= nsteps) break;
+                    const int j0 = s * kTgBlocks;
+                    const uint32_t dwp[2] = {dslot[hs].x, dslot[hs].y};
+                    if (!__all_sync(0xffffffffu, mbar_wait(&t_full[tb], tph))) {
+                        if (lane == 0) report(p.err);
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
 #pragma unroll
-                    for (int t = 0; t < 2; t++) {
-                        const int jb = 2 * pb + t;
-                        float dx[8];
-                        if (F != kTrit) {
-                            const float4 d0 = *reinterpret_cast<const float4 *>(dxf + (j0 + jb) * 8);
-                            const float4 d1 = *reinterpret_cast<const float4 *>(dxf + (j0 + jb) * 8 + 4);
-                            dx[0] = d0.x; dx[1] = d0.y; dx[2] = d0.z; dx[3] = d0.w;
-                            dx[4] = d1.x; dx[5] = d1.y; dx[6] = d1.z; dx[7] = d1.w;
+                    for (int pb = 0; pb < kTgBlocks / 2; pb++) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(tb * 128 + pb * 32), v);
+                        if (pb == kTgBlocks / 2 - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&t_empty[tb]);
                         }
 #pragma unroll
-                        for (int b = 0; b < B; b++) {
-                            // isum = 16 S_hi + S_lo, exact
-                            const float is = fmaf(16.0f, __uint_as_float(v[16 * t + b]),
-                                                  __uint_as_float(v[16 * t + 8 + b]));
-                            if (F == kTrit)
-                                acc[b] += (Acc)(int)is;
-                            else
-                                tq[b] = fmaf(dx[b], is, tq[b]);
-                        }
-                        if (F != kTrit && (jb % kBlkPerW) == kBlkPerW - 1) {
-                            const int wb = jb / kBlkPerW;  // weight block within the step
-                            const uint32_t dwb = F == kQ2 ? (wb < 2 ? dwp[0] : dwp[1]) : dwp[0];
-                            const float dw = f16_bits_to_float((uint16_t)((wb & 1) ? (dwb >> 16) : dwb));
+                        for (int t = 0; t < 2; t++) {
+                            const int jb = 2 * pb + t;
+                            float dx[8];
+                            if (F != kTrit) {
+                                const float4 d0 = *reinterpret_cast<const float4 *>(dxf + (j0 + jb) * 8);
+                                const float4 d1 = *reinterpret_cast<const float4 *>(dxf + (j0 + jb) * 8 + 4);
+                                dx[0] = d0.x; dx[1] = d0.y; dx[2] = d0.z; dx[3] = d0.w;
+                                dx[4] = d1.x; dx[5] = d1.y; dx[6] = d1.z; dx[7] = d1.w;
+                            }
 #pragma unroll
                             for (int b = 0; b < B; b++) {
-                                acc[b] = (Acc)fmaf(dw, tq[b], (float)acc[b]);
-                                tq[b] = 0.0f;
+                                // isum = 16 S_hi + S_lo, exact
+                                const float is = fmaf(16.0f, __uint_as_float(v[16 * t + b]),
+                                                      __uint_as_float(v[16 * t + 8 + b]));
+                                if (F == kTrit)
+                                    acc[b] += (Acc)(int)is;
+                                else
+                                    tq[b] = fmaf(dx[b], is, tq[b]);
+                            }
+                            if (F != kTrit && (jb % kBlkPerW) == kBlkPerW - 1) {
+                                const int wb = jb / kBlkPerW;  // weight block within the step
+                                const uint32_t dwb = F == kQ2 ? (wb < 2 ? dwp[0] : dwp[1]) : dwp[0];
+                                const float dw = f16_bits_to_float((uint16_t)((wb & 1) ? (dwb >> 16) : dwb));
+#pragma unroll
+                                for (int b = 0; b < B; b++) {
+                                    acc[b] = (Acc)fmaf(dw, tq[b], (float)acc[b]);
+                                    tq[b] = 0.0f;
+                                }
                             }
                         }
                     }
-                }
-                if (++tb == kTgAccBufs) {
-                    tb = 0;
-                    tph ^= 1;
+                    dslot[hs] = dload(s + 2);
+                    if (++tb == kTgAccBufs) {
+                        tb = 0;
+                        tph ^= 1;
+                    }
                 }
             }
             if (!ok) break;
