@@ -38,6 +38,7 @@ constexpr int kTgAStages = 3;                   // weight operand stages
 constexpr int kTgPStages = 4;                   // packed-weight stages
 constexpr int kTgMaxK = 4096;                   // K up to which the activation operand is resident
 constexpr int kTgAccBufs = 4;                   // 128-column accumulators
+constexpr uint64_t kSixteen2 = 0x4180000041800000ull;  // {16.0f, 16.0f}
 constexpr int kTgWTile = kTgRows * 32;          // one block's weight operand, e4m3: 4 KB
 constexpr int kTgXTile = 16 * 32;               // one block's activation operand: 512 B
 constexpr int kTgWStage = kTgBlocks * kTgWTile; // 32 KB
@@ -364,13 +365,20 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             const bool rv = r < M.N - row0;
             const int64_t row = row0 + (rv ? r : 0);
             typedef typename std::conditional<F == kTrit, int, float>::type Acc;
+            // Q formats at 5+ tokens: two tokens per f32x2 instruction (fewer registers made
+            // the scalar form faster at 3-4 tokens, where the paired form spills)
+            constexpr bool kPairs = F != kTrit && B >= 5;
+            constexpr int NP = (B + 1) / 2;  // token pairs
             Acc acc[B];
             float tq[B];
+            uint64_t acc2[NP], tq2[NP];      // binary32 pairs: token 2k low, 2k + 1 high
 #pragma unroll
             for (int b = 0; b < B; b++) {
                 acc[b] = 0;
                 tq[b] = 0.0f;
             }
+#pragma unroll
+            for (int k = 0; k < NP; k++) acc2[k] = tq2[k] = 0;
             // Weight scales two steps ahead in two fixed register slots (the loop is unrolled by
             // two so that no register move waits for the newest load; they come from HBM).
             auto dload = [&](int ss) {
@@ -399,41 +407,71 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int pb = 0; pb < kTgBlocks / 2; pb++) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(tb * 128 + pb * 32), v);
-                        if (pb == kTgBlocks / 2 - 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&t_empty[tb]);
-                        }
-#pragma unroll
-                        for (int t = 0; t < 2; t++) {
-                            const int jb = 2 * pb + t;
-                            float dx[8];
-                            if (F != kTrit) {
-                                const float4 d0 = *reinterpret_cast<const float4 *>(dxf + (j0 + jb) * 8);
-                                const float4 d1 = *reinterpret_cast<const float4 *>(dxf + (j0 + jb) * 8 + 4);
-                                dx[0] = d0.x; dx[1] = d0.y; dx[2] = d0.z; dx[3] = d0.w;
-                                dx[4] = d1.x; dx[5] = d1.y; dx[6] = d1.z; dx[7] = d1.w;
+                        const uint32_t taddr =
+                            tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(tb * 128 + pb * 32);
+                        if constexpr (!kPairs) {
+                            uint32_t v[32];
+                            tmem_ld32(taddr, v);
+                            if (pb == kTgBlocks / 2 - 1) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&t_empty[tb]);
                             }
 #pragma unroll
-                            for (int b = 0; b < B; b++) {
-                                // isum = 16 S_hi + S_lo, exact
-                                const float is = fmaf(16.0f, __uint_as_float(v[16 * t + b]),
-                                                      __uint_as_float(v[16 * t + 8 + b]));
-                                if (F == kTrit)
-                                    acc[b] += (Acc)(int)is;
-                                else
-                                    tq[b] = fmaf(dx[b], is, tq[b]);
-                            }
-                            if (F != kTrit && (jb % kBlkPerW) == kBlkPerW - 1) {
-                                const int wb = jb / kBlkPerW;  // weight block within the step
-                                const uint32_t dwb = F == kQ2 ? (wb < 2 ? dwp[0] : dwp[1]) : dwp[0];
-                                const float dw = f16_bits_to_float((uint16_t)((wb & 1) ? (dwb >> 16) : dwb));
+                            for (int t = 0; t < 2; t++) {
+                                const int jb = 2 * pb + t;
 #pragma unroll
                                 for (int b = 0; b < B; b++) {
-                                    acc[b] = (Acc)fmaf(dw, tq[b], (float)acc[b]);
-                                    tq[b] = 0.0f;
+                                    // isum = 16 S_hi + S_lo, exact
+                                    const float is = fmaf(16.0f, __uint_as_float(v[16 * t + b]),
+                                                          __uint_as_float(v[16 * t + 8 + b]));
+                                    if (F == kTrit)
+                                        acc[b] += (Acc)(int)is;
+                                    else
+                                        tq[b] = fmaf(dxf[(j0 + jb) * 8 + b], is, tq[b]);
+                                }
+                                if (F != kTrit && (jb % kBlkPerW) == kBlkPerW - 1) {
+                                    const int wb = jb / kBlkPerW;  // weight block within the step
+                                    const uint32_t dwb = F == kQ2 ? (wb < 2 ? dwp[0] : dwp[1]) : dwp[0];
+                                    const float dw = f16_bits_to_float((uint16_t)((wb & 1) ? (dwb >> 16) : dwb));
+#pragma unroll
+                                    for (int b = 0; b < B; b++) {
+                                        acc[b] = (Acc)fmaf(dw, tq[b], (float)acc[b]);
+                                        tq[b] = 0.0f;
+                                    }
+                                }
+                            }
+                        } else {
+                            // token pairs (2k, 2k + 1): column pair 8t + k holds their S_hi, pair
+                            // 8t + 4 + k their S_lo; two tokens per f32x2 instruction
+                            uint64_t pr[16];
+                            tmem_ld32_pairs(taddr, pr);
+                            if (pb == kTgBlocks / 2 - 1) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&t_empty[tb]);
+                            }
+#pragma unroll
+                            for (int t = 0; t < 2; t++) {
+                                const int jb = 2 * pb + t;
+                                const uint64_t *dxq = reinterpret_cast<const uint64_t *>(dxf + (j0 + jb) * 8);
+#pragma unroll
+                                for (int k = 0; k < NP; k++) {
+                                    uint64_t is2 = pr[8 * t + 4 + k];
+                                    ffma2p(is2, pr[8 * t + k], kSixteen2);  // 16 S_hi + S_lo, exact
+                                    ffma2p(tq2[k], is2, dxq[k]);            // t += d_x * isum
+                                }
+                                if ((jb % kBlkPerW) == kBlkPerW - 1) {
+                                    const int wb = jb / kBlkPerW;  // weight block within the step
+                                    const uint32_t dwb = F == kQ2 ? (wb < 2 ? dwp[0] : dwp[1]) : dwp[0];
+                                    const uint32_t dwf = __float_as_uint(
+                                        f16_bits_to_float((uint16_t)((wb & 1) ? (dwb >> 16) : dwb)));
+                                    const uint64_t dw2 = ((uint64_t)dwf << 32) | dwf;
+#pragma unroll
+                                    for (int k = 0; k < NP; k++) {
+                                        ffma2p(acc2[k], tq2[k], dw2);   // acc += d_w * t
+                                        tq2[k] = 0;
+                                    }
                                 }
                             }
                         }
@@ -446,6 +484,11 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                 }
             }
             if (!ok) break;
+            if constexpr (kPairs) {
+#pragma unroll
+                for (int b = 0; b < B; b++)
+                    acc[b] = __uint_as_float((uint32_t)(acc2[b >> 1] >> (32 * (b & 1))));
+            }
             if (rv) {
 #pragma unroll
                 for (int b = 0; b < B; b++) {
