@@ -39,6 +39,7 @@ constexpr int kTgPStages = 4;                   // packed-weight stages
 constexpr int kTgMaxK = 4096;                   // K up to which the activation operand is resident
 constexpr int kTgAccBufs = 4;                   // 128-column accumulators
 constexpr uint64_t kSixteen2 = 0x4180000041800000ull;  // {16.0f, 16.0f}
+constexpr uint64_t kOne2 = 0x3F8000003F800000ull;      // {1.0f, 1.0f}
 constexpr int kTgWTile = kTgRows * 32;          // one block's weight operand, e4m3: 4 KB
 constexpr int kTgXTile = 16 * 32;               // one block's activation operand: 512 B
 constexpr int kTgWStage = kTgBlocks * kTgWTile; // 32 KB
@@ -364,10 +365,12 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             const int row0 = (u - M.unit0) * kTgRows;
             const bool rv = r < M.N - row0;
             const int64_t row = row0 + (rv ? r : 0);
-            typedef typename std::conditional<F == kTrit, int, float>::type Acc;
-            // Q formats at 5+ tokens: two tokens per f32x2 instruction (fewer registers made
-            // the scalar form faster at 3-4 tokens, where the paired form spills)
-            constexpr bool kPairs = F != kTrit && B >= 5;
+            // Planar sums accumulate in binary32 too: every partial is an integer below
+            // 128 * K < 2^24, so they are exact and the final integer conversion is too.
+            typedef float Acc;
+            // 5+ tokens: two tokens per f32x2 instruction (the scalar form, with fewer live
+            // registers, is faster at 3-4 tokens, where the paired form spills)
+            constexpr bool kPairs = B >= 5;
             constexpr int NP = (B + 1) / 2;  // token pairs
             Acc acc[B];
             float tq[B];
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                                     const float is = fmaf(16.0f, __uint_as_float(v[16 * t + b]),
                                                           __uint_as_float(v[16 * t + 8 + b]));
                                     if (F == kTrit)
-                                        acc[b] += (Acc)(int)is;
+                                        acc[b] += is;
                                     else
                                         tq[b] = fmaf(dxf[(j0 + jb) * 8 + b], is, tq[b]);
                                 }
@@ -459,9 +462,12 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                                 for (int k = 0; k < NP; k++) {
                                     uint64_t is2 = pr[8 * t + 4 + k];
                                     ffma2p(is2, pr[8 * t + k], kSixteen2);  // 16 S_hi + S_lo, exact
-                                    ffma2p(tq2[k], is2, dxq[k]);            // t += d_x * isum
+                                    if (F == kTrit)
+                                        ffma2p(acc2[k], is2, kOne2);        // acc += isum, exact
+                                    else
+                                        ffma2p(tq2[k], is2, dxq[k]);        // t += d_x * isum
                                 }
-                                if ((jb % kBlkPerW) == kBlkPerW - 1) {
+                                if (F != kTrit && (jb % kBlkPerW) == kBlkPerW - 1) {
                                     const int wb = jb / kBlkPerW;  // weight block within the step
                                     const uint32_t dwb = F == kQ2 ? (wb < 2 ? dwp[0] : dwp[1]) : dwp[0];
                                     const uint32_t dwf = __float_as_uint(
