@@ -8,14 +8,16 @@
 //     token, S_hi and S_lo with |S| <= 32 * 2 * 15 (exact in fp32), and isum = 16 S_hi + S_lo is
 //     exact too.
 //   * The scales are applied as in the streaming GEMV: t = sum over the weight block of
-//     d_x * isum, then acc = fma(d_w, t, acc) (planar: integer sum, then the two multiplies).
+//     d_x * isum, then acc = fma(d_w, t, acc) (planar: the integer sum -- accumulated in binary32,
+//     exact below 2^24 -- then the two multiplies).
 // Why: at 8 tokens the dp4a formulation costs about four instructions per weight and cannot keep
 // up with HBM; here a weight costs about half an instruction to decode and the products run on
 // the tensor cores.
 //
 // CTA (persistent, one per SM) = 16 warps working on units of 128 weight rows x all of K, in
 // steps of 8 q8_0 blocks (256 columns).  The activation operand (hi/lo e4m3 tiles of all of K,
-// 16 K bytes) is built once per CTA by warps 1-11 and stays resident; then:
+// 16 K bytes) and the activation scales as binary32 are built once per CTA by warps 1-15 and
+// stay resident; then:
 //   warp 0      producer: one 2-D tensor copy of 128 rows x one step of packed weights per step
 //               into a 4-stage ring;
 //   warps 1-3   issue the MMAs of every third step (one thread each); warp 2 owns tensor memory;
@@ -38,6 +40,11 @@ constexpr int kTgAStages = 3;                   // weight operand stages
 constexpr int kTgPStages = 4;                   // packed-weight stages
 constexpr int kTgMaxK = 4096;                   // K up to which the activation operand is resident
 constexpr int kTgAccBufs = 4;                   // 128-column accumulators
+constexpr int kTgIssuers = 3;                   // MMA-issuing warps (1-3)
+// An issuer waits on the operand stage and accumulator of its own step; with fewer stages or
+// accumulators than issuers, two issuers would wait on phases of one barrier two apart, which a
+// parity wait cannot tell apart.
+static_assert(kTgAStages >= kTgIssuers && kTgAccBufs >= kTgIssuers, "stages per issuer");
 constexpr uint64_t kSixteen2 = 0x4180000041800000ull;  // {16.0f, 16.0f}
 constexpr uint64_t kOne2 = 0x3F8000003F800000ull;      // {1.0f, 1.0f}
 constexpr int kTgWTile = kTgRows * 32;          // one block's weight operand, e4m3: 4 KB
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
             mbar_init(&t_full[b], 1);
             mbar_init(&t_empty[b], 4);
         }
-        mbar_init(&mma_done, 3);
+        mbar_init(&mma_done, kTgIssuers);
         fence_mbar_init();
     }
     // byte lookup: int8 code -> {e4m3(code >> 4), e4m3(code & 15)}
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
         for (int i = max(0, issued - kTgPStages); i < issued; i++)
             mbar_wait(&pk_full[i % kTgPStages], (uint32_t)((i / kTgPStages) & 1));
 
-    } else if (warp >= 1 && warp <= 3) {
+    } else if (warp >= 1 && warp <= kTgIssuers) {
         // ---------------- MMA issue: warp 1 + i issues the steps g = i (mod 3) ----------------
         // (one thread each)
         if (lane == 0) {
@@ -252,7 +259,7 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                                   ? 0
                                   : ((p.nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nsteps;
             const uint32_t wbase = smem_u32(wst), xbase = smem_u32(xop);
-            for (int g = warp - 1; g < total; g += 3) {
+            for (int g = warp - 1; g < total; g += kTgIssuers) {
                 const int ai = g % kTgAStages, tb = g % kTgAccBufs;
                 if (!wait_or_report_tg(&a_full[ai], (uint32_t)((g / kTgAStages) & 1), p.err)) break;
                 if (!wait_or_report_tg(&t_empty[tb], (uint32_t)(((g / kTgAccBufs) & 1) ^ 1), p.err))
