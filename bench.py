@@ -564,6 +564,44 @@ def rows_prefill(lb, rows, stream):
         del proj, ys
         torch.cuda.empty_cache()
 
+    # (5) BitNet-2B4T-shaped prefill, planar ternary: 512 tokens through one layer's seven
+    #     projections (per-token int8 quantization of the three distinct activations + the
+    #     GEMMs; q|k|v and gate|up grouped)
+    bproj = [(synth.device_trit_planes(n, k, synth.proj_seed(95_000, 0, i)), n, k)
+             for i, (_, n, k) in enumerate(synth.BITNET_2B4T_PROJ)]
+    bks = sorted({k for _, _, k in bproj})
+    bx = {k: torch.from_numpy(synth.activations(M, k, seed=20 + k)).cuda() for k in bks}
+    bq = {k: (torch.empty((M, k), dtype=torch.int8, device="cuda"),
+              torch.empty((M,), dtype=torch.float32, device="cuda")) for k in bks}
+    bws = torch.empty(lb.lb_gemm_trit_workspace_bytes(M, max(bks)), dtype=torch.uint8,
+                      device="cuda")
+    bys = [torch.empty((M, n), dtype=torch.float32, device="cuda") for _, n, _ in bproj]
+    bops = 2 * M * sum(n * k for _, n, k in synth.BITNET_2B4T_PROJ)
+
+    def layer_planar():
+        for members in groups:
+            k = bproj[members[0]][2]
+            lb.lb_quantize_i8_absmax(bx[k], bq[k][0], bq[k][1], M, k, stream=stream)
+            lb.lb_gemm_trit_planes_grouped(
+                [(bproj[i][0], 0.02, bys[i], None, bproj[i][1]) for i in members],
+                bq[k][0], bq[k][1], M, k, bws, stream=stream)
+    ms = time_graph(Graph(layer_planar, stream), reps=20)
+    tops = bops / (ms * 1e-3) / 1e12
+    rows["bitnet_2b4t_prefill_m512_planar"] = {
+        "TOPS": round(tops, 1), "pct_tensor_peak": round(100 * tops / tflops, 1),
+        "ms_per_layer": round(ms, 4), "int8_equivalent_ops": bops,
+        "peak": f"{tflops} TFLOP/s dense bf16/f16 tensor (measured cuBLAS), the rate of the "
+                f"exact f16 tensor-core path the GEMM runs on"}
+    for i, (name, n, k) in enumerate(synth.BITNET_2B4T_PROJ):
+        def one(i=i, n=n, k=k):
+            lb.lb_gemm_trit_planes_grouped([(bproj[i][0], 0.02, bys[i], None, n)],
+                                           bq[k][0], bq[k][1], M, k, bws, stream=stream)
+        ms1 = time_graph(Graph(one, stream), reps=50)
+        rows["bitnet_2b4t_prefill_m512_planar"][f"{name}_TOPS"] = round(
+            2 * M * n * k / (ms1 * 1e-3) / 1e12, 1)
+    del bproj, bys
+    torch.cuda.empty_cache()
+
 
 # ---------------------------------------------------------------------------------------------
 # reference arm: the CPU oracle as it stands

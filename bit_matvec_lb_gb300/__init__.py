@@ -19,6 +19,9 @@ __all__ = [
     "lb_quantize_q8_0", "lb_quantize_i8_absmax", "lb_repack_q1_0", "lb_repack_q2_0_g64",
     "lb_gemv_q1_0", "lb_gemv_q2_0_g64", "lb_gemv_trit_planes", "lb_gemv_bf16",
     "lb_gemv_q1_0_grouped", "lb_gemv_q2_0_g64_grouped", "lb_gemv_trit_planes_grouped",
+    "lb_gemm_workspace_bytes", "lb_gemm_q1_0", "lb_gemm_q2_0_g64", "lb_gemm_q1_0_grouped",
+    "lb_gemm_q2_0_g64_grouped", "lb_gemm_q2_0_g64_noalloc", "lb_gemm_trit_workspace_bytes",
+    "lb_gemm_trit_planes", "lb_gemm_trit_planes_grouped",
 ]
 
 LB_STATUS = {0: "LB_OK", -1: "LB_ERR_NULL", -2: "LB_ERR_ALIGN", -3: "LB_ERR_SHAPE",
@@ -85,6 +88,10 @@ SIGNATURES = {
                                    ctypes.c_size_t, P]),
     "lb_gemm_q2_0_g64_grouped": (I32, [ctypes.POINTER(lb_gemm_matrix), I32, P, P, I64, I64, P,
                                        ctypes.c_size_t, P]),
+    "lb_gemm_trit_workspace_bytes": (ctypes.c_size_t, [I64, I64]),
+    "lb_gemm_trit_planes": (I32, [P, F32, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
+    "lb_gemm_trit_planes_grouped": (I32, [ctypes.POINTER(lb_trit_matrix), I32, P, P, I64, I64, P,
+                                          ctypes.c_size_t, P]),
 }
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -302,3 +309,35 @@ def lb_gemm_q2_0_g64_noalloc(codes, scales, q, d, y, M: int, N: int, K: int, str
     _check("lb_gemm_q2_0_g64_noalloc", load().lb_gemm_q2_0_g64_noalloc(
         _ptr(codes), _ptr(scales), _ptr(q), _ptr(d), _ptr(y), int(M), int(N), int(K),
         _stream(stream)))
+
+
+def lb_gemm_trit_workspace_bytes(M: int, K: int) -> int:
+    """Bytes of device scratch lb_gemm_trit_planes* needs for M tokens of K columns."""
+    return int(load().lb_gemm_trit_workspace_bytes(int(M), int(K)))
+
+
+def lb_gemm_trit_planes(planes, w_scale: float, q, x_scale, y, acc, M: int, N: int, K: int,
+                        workspace, workspace_bytes=None, stream=None):
+    """Planar ternary prefill GEMM; workspace: a device tensor (its size is passed) or a
+    pointer with workspace_bytes."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("lb_gemm_trit_planes", load().lb_gemm_trit_planes(
+        _ptr(planes), float(w_scale), _ptr(q), _ptr(x_scale), _ptr(y), _ptr(acc), int(M),
+        int(N), int(K), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def lb_gemm_trit_planes_grouped(mats, q, x_scale, M: int, K: int, workspace,
+                                workspace_bytes=None, stream=None):
+    """mats: sequence of (planes, w_scale, y, acc_or_None, N) sharing the activation (one
+    launch)."""
+    if not 1 <= len(mats) <= GEMM_MAX_GROUP:
+        raise ValueError(f"a GEMM group holds 1..{GEMM_MAX_GROUP} matrices")
+    arr = (lb_trit_matrix * len(mats))()
+    for i, (planes, w_scale, y, acc, N) in enumerate(mats):
+        arr[i] = lb_trit_matrix(_ptr(planes), float(w_scale), _ptr(y), _ptr(acc), int(N))
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("lb_gemm_trit_planes_grouped", load().lb_gemm_trit_planes_grouped(
+        arr, len(mats), _ptr(q), _ptr(x_scale), int(M), int(K), _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))

@@ -28,6 +28,8 @@
 //     activation tiles, warp 5 owns tensor memory and issues the MMAs (one thread), warps 8-15
 //     (two warpgroups) drain.  A 4-stage shared-memory ring of {A tile, B tile} decouples them;
 //     every wait is bounded and reports through the device error word.
+#include <algorithm>
+
 #include "lb_tc.cuh"
 
 namespace lb {
@@ -71,15 +73,19 @@ struct GemmParams {
 // interleave of two source words:  Q2_0_g64 words (4(kc/2) + kc%2, +2), Q1_0 words (kc, kc+4).
 // Rows past M are zero.  One thread per (tile row, K32 block), rows fastest.
 // ------------------------------------------------------------------------------------------
+// `zero` (nzero ints, may be NULL) is cleared as well: the planar GEMM's split counters.
 template <int F>
 __global__ void __launch_bounds__(256) gemm_prep_act_kernel(const int8_t *__restrict__ q,
                                                             uint8_t *__restrict__ ws, int M,
-                                                            int K, int mtiles) {
+                                                            int K, int mtiles, int *zero,
+                                                            int nzero) {
     pdl_launch_dependents();
     pdl_wait();
     const int nK32 = K / 32;
     const int64_t total = (int64_t)mtiles * nK32 * kTileM;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += stride)
+        zero[i] = 0;
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
         const int r = (int)(i % kTileM);
@@ -465,9 +471,11 @@ static int gemm_q_group(int F, const lb_gemm_matrix *mats, int G, const int8_t *
     int64_t pgrid = (work + 255) / 256;
     if (pgrid > (int64_t)di.sms * 16) pgrid = (int64_t)di.sms * 16;
     int e = F == kG1 ? launch_pdl(gemm_prep_act_kernel<kG1>, dim3((unsigned)pgrid), dim3(256), 0,
-                                  st, q, (uint8_t *)workspace, (int)M, (int)K, (int)mtiles)
+                                  st, q, (uint8_t *)workspace, (int)M, (int)K, (int)mtiles,
+                                  (int *)nullptr, 0)
                      : launch_pdl(gemm_prep_act_kernel<kG2>, dim3((unsigned)pgrid), dim3(256), 0,
-                                  st, q, (uint8_t *)workspace, (int)M, (int)K, (int)mtiles);
+                                  st, q, (uint8_t *)workspace, (int)M, (int)K, (int)mtiles,
+                                  (int *)nullptr, 0);
     if (e) return e;
     p.ws = (const uint8_t *)workspace;
     p.d = d;
@@ -536,3 +544,427 @@ int gemm_q_with_workspace(int q2, const uint8_t *bits, const uint16_t *scales, c
                   stream);
 }
 }  // namespace lb
+
+
+// ==========================================================================================
+// Planar ternary prefill GEMM (tritium.technology "Architecture", sections 1, 2, 4.1 and 5 for
+// the arithmetic; the bankml technical report, III.3, for the prefill tile that reuses one
+// weight tile across many tokens).  For token m and weight row n:
+//     acc[m][n] = sum_{c: pos} q[m][c] - sum_{c: neg} q[m][c]        (int32, exact)
+//     y[m][n]   = (float(acc) * x_scale[m]) * w_scale                  (two roundings)
+//
+// GPU design.  Activations are the same f16 operand tiles as the Q1_0 GEMM (its prologue and
+// K permutation); weights are expanded in shared memory to f16 -1 / 0 / +1.  Every partial sum
+// of the tensor core is an integer of magnitude at most 128 K < 2^24, exact in the binary32
+// accumulator whatever the order of the additions, so one tensor-memory accumulator runs over
+// the whole of K and is read once at the end: no per-block drain.  For the same reason K may
+// be split across CTAs with no effect on the result: a call whose tiles would leave SMs idle
+// runs the ks splits of each tile as one thread-block cluster; every split parks its integer
+// partial tile in its own shared memory, and after a cluster barrier each CTA adds 1/ks of the
+// tile's columns over the whole cluster (distributed shared memory) and writes those outputs.
+//   Warp roles in a 192-thread CTA (two CTAs per SM): warps 0-3 expand weights (thread = weight
+//   row) and then read the accumulator out (thread = token = tensor-memory lane), warp 4 copies
+//   activation tiles, warp 5 owns tensor memory and issues the MMAs.  Three stages of one
+//   64-column beat each; every mbarrier wait is bounded and reports through the device error
+//   word.  The two cluster barriers are reached by every thread of every CTA on every path.
+// ==========================================================================================
+namespace lb {
+
+constexpr int kTritThreads = 192;
+constexpr int kTritStages = 3;
+constexpr int kTritSmem = kTritStages * kStageBytes + 1024;
+constexpr int kTritSplitCtas = 304;        // split K while fewer CTAs than this would run
+constexpr int kTritMaxSplit = 4;           // cluster size (portable limit: 8)
+constexpr int kTritMinStages = 4;          // beats per split, at least
+constexpr int kPartPitch = kTileN + 4;     // partial tile [m][n] row pitch (conflict-free)
+static_assert(kTileM * kPartPitch * 4 <= kTritStages * kStageBytes,
+              "the partial tile must fit in the stage ring");
+
+struct TritGemmMat {
+    const uint4 *planes;     // [N][K/64] beats {pos lo, pos hi, neg lo, neg hi}
+    float *y;                // [M][N]
+    int32_t *acc;            // [M][N] or NULL
+    float w_scale;
+    int N, tile0;
+};
+
+struct TritGemmParams {
+    TritGemmMat mat[LB_GEMM_MAX_GROUP];
+    const uint8_t *ws;       // activation tiles [mtiles][K/32][8192 B]
+    const float *x_scale;    // [M]
+    int *err;
+    int G, M, nst, mtiles, ks, sps;
+};
+
+// Half a planar beat -- pos word P and neg word Nn of 32 columns, bit c <-> column c -- as the
+// four 16-byte chunks of one weight row of a 32-deep operand tile.  f16x2 number i (0..15) holds
+// the weights of columns (i, i + 16), the pairing of the Q1_0 activation tiles.  The 2-bit value
+// 1 + p - n (0, 1 or 2) of every column is formed for the even and for the odd columns in one
+// addition each; field s of the even word is column 2s (high half: 2s + 16), and
+// (1024 + f) - 1025 = p - n in f16.
+__device__ __forceinline__ void expand_trit(uint32_t P, uint32_t Nn, uint4 (&c)[4]) {
+    constexpr uint32_t kEven = 0x55555555u;
+    const uint32_t fe = (P & kEven) + (~Nn & kEven);
+    const uint32_t fo = ((P >> 1) & kEven) + ((~Nn >> 1) & kEven);
+    const __half2 k1025 = __halves2half2(__ushort_as_half(0x6401), __ushort_as_half(0x6401));
+    uint32_t o[16];
+#pragma unroll
+    for (int s = 0; s < 8; s++) {
+        uint32_t xe = ((fe >> (2 * s)) & 0x00030003u) | 0x64006400u;
+        uint32_t xo = ((fo >> (2 * s)) & 0x00030003u) | 0x64006400u;
+        __half2 ve = __hsub2(*reinterpret_cast<__half2 *>(&xe), k1025);
+        __half2 vo = __hsub2(*reinterpret_cast<__half2 *>(&xo), k1025);
+        o[2 * s] = *reinterpret_cast<uint32_t *>(&ve);
+        o[2 * s + 1] = *reinterpret_cast<uint32_t *>(&vo);
+    }
+#pragma unroll
+    for (int kc = 0; kc < 4; kc++)
+        c[kc] = make_uint4(o[4 * kc], o[4 * kc + 1], o[4 * kc + 2], o[4 * kc + 3]);
+}
+
+// Cluster barrier over every thread of every CTA of the cluster (release / acquire: shared
+// memory written before it is visible to the whole cluster after it).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Four consecutive floats of CTA `rank`'s shared memory at the address this CTA uses for them.
+__device__ __forceinline__ float4 ld_cluster_f4(const float *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)),
+                 "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+
+// The 32 outputs of token row m (yrow / arow point at its row) for weight rows nb .. nb + 31,
+// from their exact integer accumulators a[].
+__device__ __forceinline__ void trit_store32(const float (&a)[32], float xs, float w_scale,
+                                             float *yrow, int32_t *arow, int64_t nb, int N) {
+    float o[32];
+#pragma unroll
+    for (int j = 0; j < 32; j++) o[j] = __fmul_rn(__fmul_rn(a[j], xs), w_scale);
+    if ((N & 3) == 0 && nb + 32 <= N) {
+#pragma unroll
+        for (int v = 0; v < 8; v++)
+            reinterpret_cast<float4 *>(yrow + nb)[v] =
+                make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+        if (arow) {
+#pragma unroll
+            for (int v = 0; v < 8; v++)
+                reinterpret_cast<int4 *>(arow + nb)[v] = make_int4(
+                    __float2int_rn(a[4 * v]), __float2int_rn(a[4 * v + 1]),
+                    __float2int_rn(a[4 * v + 2]), __float2int_rn(a[4 * v + 3]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+            if (nb + j < N) {
+                yrow[nb + j] = o[j];
+                if (arow) arow[nb + j] = __float2int_rn(a[j]);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kTritThreads, 2)
+    gemm_trit_kernel(const __grid_constant__ TritGemmParams p) {
+    extern __shared__ uint8_t gsm_raw[];
+    uint8_t *gsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) &
+                                               ~(uintptr_t)1023);
+    // full[s]: the stage's two activation tiles have landed and its two weight tiles are written.
+    // empty[s]: the stage's four MMAs have completed (the stage may be refilled).
+    // mma_done: every MMA of the CTA has completed (the accumulator may be read).
+    __shared__ __align__(8) uint64_t full[kTritStages], empty[kTritStages], mma_done;
+    __shared__ uint32_t tmem_slot;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = (int)blockIdx.x / p.ks, split = (int)blockIdx.x % p.ks;  // split = rank
+    int gi = 0;
+    while (gi + 1 < p.G && p.mat[gi + 1].tile0 <= tile) gi++;
+    const TritGemmMat &W = p.mat[gi];
+    const int m_tile = (tile - W.tile0) % p.mtiles;
+    const int n_tile = (tile - W.tile0) / p.mtiles;
+    const int64_t m0 = (int64_t)m_tile * kTileM, n0 = (int64_t)n_tile * kTileN;
+    const int sb = split * p.sps;                 // first beat of this split
+    const int nloc = min(p.nst, sb + p.sps) - sb;  // beats of this split (>= 1 by construction)
+    float *part = reinterpret_cast<float *>(gsm);  // partial tile, once the ring is idle
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTritStages; s++) {
+            mbar_init(&full[s], 5);   // four expander warps + the activation copy (and its bytes)
+            mbar_init(&empty[s], 1);  // commit after the stage's MMAs
+        }
+        mbar_init(&mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(&tmem_slot, kTileN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    pdl_launch_dependents();
+
+    // token row of the epilogue threads (warps 0-3 = tensor-memory lane quarters)
+    const int mrow = threadIdx.x;
+    const int64_t m = m0 + mrow;
+    const bool mvalid = warp < 4 && m < p.M;
+    float xs = 0.f;
+
+    if (warp < 4) {
+        // ---------------- weight expanders: thread = weight row ----------------
+        // Beats are read kQ stages ahead into a register queue with one fixed slot per stage of
+        // the unrolled loop.
+        constexpr int kQ = 4;
+        const int nl = threadIdx.x;
+        const int64_t n = n0 + nl;
+        const bool valid = n < W.N;
+        const uint4 *row = W.planes + (valid ? n : 0) * (int64_t)p.nst + sb;
+        auto load_beat = [&](int i) -> uint4 {
+            return (valid && i < nloc) ? row[i] : make_uint4(0, 0, 0, 0);
+        };
+        uint4 qb[kQ];
+#pragma unroll
+        for (int i = 0; i < kQ; i++) qb[i] = load_beat(i);
+        const uint32_t boff = (uint32_t)canon_offset(nl, 0) + 2 * kTileBytes;
+        Ring<kTritStages> rs;
+        bool ok = true;
+        for (int i0 = 0; i0 < nloc && ok; i0 += kQ) {
+#pragma unroll
+            for (int j = 0; j < kQ; j++) {
+                const int i = i0 + j;
+                if (i >= nloc) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[rs.idx], rs.phase ^ 1u))) {
+                    if (lane == 0) atomicOr(p.err, 1);
+                    ok = false;
+                    break;
+                }
+                uint8_t *bt = gsm + rs.idx * kStageBytes + boff;
+#pragma unroll
+                for (int t = 0; t < 2; t++) {
+                    uint4 c[4];
+                    expand_trit(t ? qb[j].y : qb[j].x, t ? qb[j].w : qb[j].z, c);
+#pragma unroll
+                    for (int kc = 0; kc < 4; kc++)
+                        *reinterpret_cast<uint4 *>(bt + t * kTileBytes + kc * kCoreLBO) = c[kc];
+                }
+                qb[j] = load_beat(i + kQ);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[rs.idx]);
+                rs.next();
+            }
+        }
+
+        // ---------------- accumulator read-out: thread = token (tensor-memory lane) ----------
+        pdl_wait();
+        xs = mvalid ? p.x_scale[m] : 0.f;
+        if (!__all_sync(0xffffffffu, mbar_wait(&mma_done, 0)) && lane == 0) atomicOr(p.err, 1);
+        tc_fence_after();
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        float *yrow = W.y + (mvalid ? m : 0) * (int64_t)W.N;
+        int32_t *arow = W.acc ? W.acc + (mvalid ? m : 0) * (int64_t)W.N : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < kTileN / 32; c++) {
+            uint32_t r[32];
+            __syncwarp();  // the tensor-memory load is warp-collective
+            tmem_ld32(tl + 32 * c, r);
+            if (p.ks > 1) {
+                // every MMA has completed, so the stage ring is idle: park the partial there
+                float4 *dst = reinterpret_cast<float4 *>(part + mrow * kPartPitch + 32 * c);
+#pragma unroll
+                for (int v = 0; v < 8; v++)
+                    dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                         __uint_as_float(r[4 * v + 2]),
+                                         __uint_as_float(r[4 * v + 3]));
+            } else if (mvalid) {
+                float a[32];
+#pragma unroll
+                for (int j = 0; j < 32; j++) a[j] = __uint_as_float(r[j]);
+                trit_store32(a, xs, W.w_scale, yrow, arow, n0 + 32 * c, W.N);
+            }
+        }
+    } else if (warp == 4) {
+        // ---------------- activation tiles: one 16 KB bulk copy per stage ----------------
+        pdl_wait();
+        if (lane == 0) {
+            const uint8_t *src = p.ws + ((int64_t)m_tile * p.nst + sb) * 2 * kTileBytes;
+            Ring<kTritStages> rs;
+            int issued = 0;
+            for (int i = 0; i < nloc; i++) {
+                if (!wait_or_report(&empty[rs.idx], rs.phase ^ 1u, p.err)) break;
+                mbar_arrive_expect_tx(&full[rs.idx], 2 * kTileBytes);
+                bulk_g2s(gsm + rs.idx * kStageBytes, src + (int64_t)i * 2 * kTileBytes,
+                         2 * kTileBytes, &full[rs.idx]);
+                rs.next();
+                issued = i + 1;
+            }
+            // No copy may still be landing in shared memory when the ring is reused or the CTA
+            // exits.
+            for (int i = max(0, issued - kTritStages); i < issued; i++)
+                mbar_wait(&full[i % kTritStages], (uint32_t)(i / kTritStages) & 1u);
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issue: one thread, one accumulator over the split's K ----------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(kTileM, kTileN);
+            const uint32_t sbase = smem_u32(gsm);
+            Ring<kTritStages> rs;
+            for (int i = 0; i < nloc; i++) {
+                if (!wait_or_report(&full[rs.idx], rs.phase, p.err)) break;
+                tc_fence_after();
+                const uint32_t sa = sbase + (uint32_t)(rs.idx * kStageBytes);
+#pragma unroll
+                for (int t = 0; t < 2; t++) {
+                    const uint64_t ad = smem_desc(sa + t * kTileBytes);
+                    const uint64_t bd = smem_desc(sa + (2 + t) * kTileBytes);
+                    mma_f16(tmem, ad, bd, idesc, (i | t) ? 1u : 0u);
+                    mma_f16(tmem, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);
+                }
+                mma_commit(&empty[rs.idx]);
+                rs.next();
+            }
+            mma_commit(&mma_done);
+            wait_or_report(&mma_done, 0, p.err);
+        }
+    }
+
+    if (p.ks > 1) {
+        // Split tiles: every CTA of the cluster has parked its partial tile (every thread of
+        // every CTA arrives here once, whatever its role).  CTA `split` then adds the column
+        // chunks c = split, split + ks, ... over the cluster and writes their outputs; the second
+        // barrier keeps every partial alive until all CTAs have read it.
+        __syncwarp();
+        cluster_sync_all();
+        if (warp < 4) {
+            float *yrow = W.y + (mvalid ? m : 0) * (int64_t)W.N;
+            int32_t *arow = W.acc ? W.acc + (mvalid ? m : 0) * (int64_t)W.N : nullptr;
+            for (int c = split; c < kTileN / 32; c += p.ks) {
+                float a[32];
+#pragma unroll
+                for (int j = 0; j < 32; j++) a[j] = 0.f;
+                const float *src = part + mrow * kPartPitch + 32 * c;
+                // integer partials: every sum stays an integer below 2^24, exact in any order
+                for (int s = 0; s < p.ks; s++) {
+#pragma unroll
+                    for (int v = 0; v < 8; v++) {
+                        const float4 t = ld_cluster_f4(src + 4 * v, (uint32_t)s);
+                        a[4 * v] += t.x;
+                        a[4 * v + 1] += t.y;
+                        a[4 * v + 2] += t.z;
+                        a[4 * v + 3] += t.w;
+                    }
+                }
+                if (mvalid) trit_store32(a, xs, W.w_scale, yrow, arow, n0 + 32 * c, W.N);
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTileN);
+    }
+}
+
+static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
+                           const float *x_scale, int64_t M, int64_t K, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (!mats || !q || !x_scale || !workspace) return LB_ERR_NULL;
+    if (G < 1 || G > LB_GEMM_MAX_GROUP) return LB_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(x_scale) || !aligned16(workspace)) return LB_ERR_ALIGN;
+    if (M < 1 || M > (1 << 30) || K < 64 || K % 64 != 0 || K > (1 << 24) / 128)
+        return LB_ERR_SHAPE;
+    if (workspace_bytes < lb_gemm_workspace_bytes(M, K)) return LB_ERR_SHAPE;
+    const int64_t mtiles = (M + kTileM - 1) / kTileM;
+    TritGemmParams p{};
+    int64_t tiles = 0;
+    for (int i = 0; i < G; i++) {
+        const lb_trit_matrix &m = mats[i];
+        if (!m.planes || !m.y) return LB_ERR_NULL;
+        if (!aligned16(m.planes) || !aligned16(m.y) || (m.acc_opt && !aligned16(m.acc_opt)))
+            return LB_ERR_ALIGN;
+        if (m.N < 1 || m.N > (1 << 30)) return LB_ERR_SHAPE;
+        p.mat[i].planes = reinterpret_cast<const uint4 *>(m.planes);
+        p.mat[i].y = m.y;
+        p.mat[i].acc = m.acc_opt;
+        p.mat[i].w_scale = m.w_scale;
+        p.mat[i].N = (int)m.N;
+        p.mat[i].tile0 = (int)tiles;
+        tiles += mtiles * ((m.N + kTileN - 1) / kTileN);
+        if (tiles > 0x7fffffff / kTritMaxSplit) return LB_ERR_SHAPE;
+    }
+    const int nst = (int)(K / 64);
+    // Split K when the tiles alone would leave SMs idle (ks * tiles <= kTritSplitCtas), with at
+    // least kTritMinStages beats per split and no split empty.
+    int ks = (int)std::min<int64_t>(kTritMaxSplit, std::max<int64_t>(1, kTritSplitCtas / tiles));
+    ks = std::min(ks, std::max(1, nst / kTritMinStages));
+    const int sps = (nst + ks - 1) / ks;
+    ks = (nst + sps - 1) / sps;
+    DeviceInfo di;
+    if (int st = current_device_info(&di)) return st;
+    cudaStream_t st = as_stream(stream);
+    const int64_t work = mtiles * kTileM * (K / 32);
+    int64_t pgrid = (work + 255) / 256;
+    if (pgrid > (int64_t)di.sms * 16) pgrid = (int64_t)di.sms * 16;
+    if (int e = launch_pdl(gemm_prep_act_kernel<kG1>, dim3((unsigned)pgrid), dim3(256), 0, st, q,
+                           (uint8_t *)workspace, (int)M, (int)K, (int)mtiles, (int *)nullptr, 0))
+        return e;
+    p.ws = static_cast<const uint8_t *>(workspace);
+    p.x_scale = x_scale;
+    p.err = device_error_word();
+    p.G = G;
+    p.M = (int)M;
+    p.nst = nst;
+    p.mtiles = (int)mtiles;
+    p.ks = ks;
+    p.sps = sps;
+    int bps = 0;
+    if (int e = prepare_kernel(reinterpret_cast<const void *>(gemm_trit_kernel), kTritThreads,
+                               kTritSmem, &bps))
+        return e;
+    // The ks splits of a tile are consecutive blocks and form one cluster.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles * ks));
+    cfg.blockDim = dim3(kTritThreads);
+    cfg.dynamicSmemBytes = kTritSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)ks;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_trit_kernel, p);
+    if (e == cudaSuccess) return LB_OK;
+    record_cuda_error(e);
+    return LB_ERR_LAUNCH;
+}
+
+}  // namespace lb
+
+LB_EXPORT size_t lb_gemm_trit_workspace_bytes(int64_t M, int64_t K) {
+    return lb_gemm_workspace_bytes(M, K);
+}
+
+LB_EXPORT int lb_gemm_trit_planes_grouped(const lb_trit_matrix *mats, int G, const int8_t *q,
+                                          const float *x_scale, int64_t M, int64_t K,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+    return gemm_trit_group(mats, G, q, x_scale, M, K, workspace, workspace_bytes, stream);
+}
+
+LB_EXPORT int lb_gemm_trit_planes(const uint64_t *planes, float w_scale, const int8_t *q,
+                                  const float *x_scale, float *y, int32_t *acc_opt, int64_t M,
+                                  int64_t N, int64_t K, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    const lb_trit_matrix m = {planes, w_scale, y, acc_opt, N};
+    return gemm_trit_group(&m, 1, q, x_scale, M, K, workspace, workspace_bytes, stream);
+}

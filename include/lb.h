@@ -248,6 +248,42 @@ int lb_gemm_q2_0_g64_grouped(const lb_gemm_matrix *mats, int G, const int8_t *q,
                              const uint16_t *d, int64_t M, int64_t K, void *workspace,
                              size_t workspace_bytes, void *stream);
 
+/* ---- Planar ternary prefill GEMM ([TA] 1, 2, 4.1, 5 for the arithmetic; [TR] III.3 for the
+ * prefill tile that reuses one weight tile across many tokens).  lb_gemv_trit_planes for each
+ * of M tokens:
+ *   acc[m][n] = sum_{c: pos bit set} q[m][c] - sum_{c: neg bit set} q[m][c]   (int32, exact)
+ *   y[m][n]   = (float(acc) * x_scale[m]) * w_scale    (two binary32 roundings, in this order)
+ * computed on the tensor cores with exact integer sums, so acc and y are bit-identical to the
+ * GEMV's for the same token.
+ *   planes    : [N][K/64][2] u64 {pos, neg} beats (layout of lb_gemv_trit_planes).
+ *   q         : [M][K] int8 (for example lb_quantize_i8_absmax).   x_scale : [M] fp32.
+ *   y         : [M][N] fp32, overwritten.   acc_opt : NULL, or [M][N] int32 that receives acc.
+ *   workspace : device scratch of at least lb_gemm_trit_workspace_bytes(M, K) bytes (the same
+ *               size as lb_gemm_workspace_bytes), owned by the caller and rewritten by every
+ *               call with the activations in the tensor-core operand layout; it must not be
+ *               used by another call that may run at the same time.  Its contents need no
+ *               initialization.
+ * Calls with few tiles split K across the CTAs of a thread-block cluster; the integer partial
+ * sums are added exactly, so the split never changes a result.
+ * Limits: 1 <= M, N <= 2^30; K % 64 == 0, 64 <= K <= 2^24 / 128 (so |acc| <= 2^24 and every
+ * partial sum is exact in binary32).  A column set in both planes gives an unspecified result.
+ * Errors: LB_ERR_NULL, LB_ERR_ALIGN, LB_ERR_SHAPE (limits, or a workspace too small),
+ * LB_ERR_ARCH, LB_ERR_LAUNCH; a bounded wait that gives up sets the device status. */
+size_t lb_gemm_trit_workspace_bytes(int64_t M, int64_t K);  /* 0 for M < 1 or K < 1 */
+
+int lb_gemm_trit_planes(const uint64_t *planes, float w_scale, const int8_t *q,
+                        const float *x_scale, float *y, int32_t *acc_opt, int64_t M, int64_t N,
+                        int64_t K, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Grouped planar prefill GEMM: mats[0..G-1] (host array of lb_trit_matrix, 1 <= G <=
+ * LB_GEMM_MAX_GROUP, read during the call) against ONE activation q, x_scale of M tokens, in one
+ * launch (for example q, k and v, or gate and up).  Same arithmetic, limits, workspace and
+ * errors as lb_gemm_trit_planes; each matrix has its own rows N, w_scale, output y [M][N] and
+ * optional acc [M][N]; outputs must not overlap. */
+int lb_gemm_trit_planes_grouped(const lb_trit_matrix *mats, int G, const int8_t *q,
+                                const float *x_scale, int64_t M, int64_t K, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
 /* ---- Q2_0_g64 prefill GEMM without caller scratch.
  * No counterpart in the source pages: a convenience of this library for callers that cannot
  * allocate device memory.  Same arithmetic, accuracy, layouts and errors as lb_gemm_q2_0_g64,

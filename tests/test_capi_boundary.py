@@ -200,3 +200,43 @@ def test_gemm_refusals(lib, fn, qk):
         assert f(A, A, A, A, A, M, N, K, A, 2**40, None) == -3
     # workspace one byte short
     assert f(A, A, A, A, A, 16, 8, 4 * qk, A, ws - 1, None) == -3
+
+
+# ---- planar prefill GEMM: host checks ----
+def test_gemm_trit_workspace_bytes(lib):
+    assert lib.lb_gemm_trit_workspace_bytes(0, 64) == 0
+    assert lib.lb_gemm_trit_workspace_bytes(1, 0) == 0
+    # the activation tiles of the Q GEMMs, nothing else
+    for M, K in ((1, 64), (130, 2560), (512, 6912)):
+        assert lib.lb_gemm_trit_workspace_bytes(M, K) == lib.lb_gemm_workspace_bytes(M, K)
+
+
+def test_gemm_trit_refusals(lib):
+    f = lib.lb_gemm_trit_planes
+    K = 256
+    ws = lib.lb_gemm_trit_workspace_bytes(16, K)
+    ok = [A, 1.0, A, A, A, None, 16, 8, K, A, ws, None]
+    for i in (0, 2, 3, 4, 9):
+        args = list(ok)
+        args[i] = None
+        assert f(*args) == -1
+    for i in (0, 2, 3, 4, 5, 9):
+        args = list(ok)
+        args[i] = MIS
+        assert f(*args) == -2
+    for M, N, KK in ((0, 8, K), (16, 0, K), (16, 8, 32), (16, 8, K + 32), (16, 8, 0),
+                     (2**31, 8, K), (16, 8, (1 << 24) // 128 + 64)):
+        assert f(A, 1.0, A, A, A, None, M, N, KK, A, 2**40, None) == -3
+    assert f(A, 1.0, A, A, A, None, 16, 8, K, A, ws - 1, None) == -3   # workspace short
+    g = lib.lb_gemm_trit_planes_grouped
+    arr = (lb.lb_trit_matrix * 9)()
+    for i in range(9):
+        arr[i] = lb.lb_trit_matrix(A, 1.0, A, None, 8)
+    assert g(arr, 0, A, A, 16, K, A, ws, None) == -3      # empty group
+    assert g(arr, 9, A, A, 16, K, A, ws, None) == -3      # more than LB_GEMM_MAX_GROUP
+    arr[1] = lb.lb_trit_matrix(None, 1.0, A, None, 8)
+    assert g(arr, 2, A, A, 16, K, A, ws, None) == -1      # NULL planes of matrix 1
+    arr[1] = lb.lb_trit_matrix(A, 1.0, A, MIS, 8)
+    assert g(arr, 2, A, A, 16, K, A, ws, None) == -2      # misaligned acc of matrix 1
+    arr[1] = lb.lb_trit_matrix(A, 1.0, A, None, 0)
+    assert g(arr, 2, A, A, 16, K, A, ws, None) == -3      # N = 0
