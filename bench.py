@@ -411,6 +411,7 @@ def rows_measure(lb, out, which: str = "all"):
     rows = {}
     if which in ("all", "decode"):
         rows_decode(lb, rows, stream)
+        rows_dequant(lb, rows, stream)
     if which in ("all", "prefill"):
         rows_prefill(lb, rows, stream)
     out["rows"] = rows
@@ -524,6 +525,39 @@ def rows_decode(lb, rows, stream):
             "ms_per_token": round(ms, 4), "bytes": tot,
             "head_GB/s": round(HN * HK * 2 / (ms_head * 1e-3) / 1e9, 1),
             "body_GB/s": round(body_bytes / ((ms - ms_head) * 1e-3) / 1e9, 1)}
+
+
+def rows_dequant(lb, rows, stream):
+    import torch
+    import synth
+    hbm, _ = peaks()
+    # (6) load-time dequantization, HBM-bound: 16 distinct 4096 x 4096 matrices per pass
+    #     (> L2), Q2_0_g64 and planar, to fp32 and bf16; bytes = packed weights + scales read
+    #     + outputs written
+    N, K, R = ROWS_N, ROWS_K, 16
+    Wq = [make_q2_weights(N, K, 96_000 + r) for r in range(R)]
+    Wt = [synth.device_trit_planes(N, K, 97_000 + r) for r in range(R)]
+    for fmt, esz in ((lb.OUT_F32, 4), (lb.OUT_BF16, 2)):
+        out = torch.empty((N, K), dtype=torch.float32 if esz == 4 else torch.int16,
+                          device="cuda")
+        name = "f32" if esz == 4 else "bf16"
+
+        def q2pass():
+            for c, s in Wq:
+                lb.lb_dequantize_q2_0_g64(c, s, N, K, fmt, out, stream=stream)
+
+        def tpass():
+            for t in Wt:
+                lb.lb_dequantize_trit_planes(t, 0.02, N, K, fmt, out, stream=stream)
+        for label, fn, wbytes in (("q2_0_g64", q2pass, q2_bytes(N, K) + N * scale_stride(K, 64) * 2 - N * (K // 64) * 2),
+                                  ("trit_planes", tpass, N * K // 64 * 16)):
+            ms = time_graph(Graph(fn, stream), reps=20) / R
+            gbs = (wbytes + N * K * esz) / (ms * 1e-3) / 1e9
+            rows[f"dequant_{label}_4096x4096_{name}"] = {
+                "GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
+                "us_per_matrix": round(ms * 1e3, 2)}
+    del Wq, Wt
+    torch.cuda.empty_cache()
 
 
 def rows_prefill(lb, rows, stream):

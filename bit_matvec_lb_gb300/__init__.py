@@ -21,7 +21,8 @@ __all__ = [
     "lb_gemv_q1_0_grouped", "lb_gemv_q2_0_g64_grouped", "lb_gemv_trit_planes_grouped",
     "lb_gemm_workspace_bytes", "lb_gemm_q1_0", "lb_gemm_q2_0_g64", "lb_gemm_q1_0_grouped",
     "lb_gemm_q2_0_g64_grouped", "lb_gemm_q2_0_g64_noalloc", "lb_gemm_trit_workspace_bytes",
-    "lb_gemm_trit_planes", "lb_gemm_trit_planes_grouped",
+    "lb_gemm_trit_planes", "lb_gemm_trit_planes_grouped", "lb_dequantize_q1_0",
+    "lb_dequantize_q2_0_g64", "lb_dequantize_trit_planes", "OUT_F32", "OUT_BF16",
 ]
 
 LB_STATUS = {0: "LB_OK", -1: "LB_ERR_NULL", -2: "LB_ERR_ALIGN", -3: "LB_ERR_SHAPE",
@@ -92,7 +93,13 @@ SIGNATURES = {
     "lb_gemm_trit_planes": (I32, [P, F32, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
     "lb_gemm_trit_planes_grouped": (I32, [ctypes.POINTER(lb_trit_matrix), I32, P, P, I64, I64, P,
                                           ctypes.c_size_t, P]),
+    "lb_dequantize_q1_0": (I32, [P, P, I64, I64, I32, P, P]),
+    "lb_dequantize_q2_0_g64": (I32, [P, P, I64, I64, I32, P, P]),
+    "lb_dequantize_trit_planes": (I32, [P, F32, I64, I64, I32, P, P]),
 }
+
+OUT_F32 = 0
+OUT_BF16 = 1
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -341,3 +348,21 @@ def lb_gemm_trit_planes_grouped(mats, q, x_scale, M: int, K: int, workspace,
     _check("lb_gemm_trit_planes_grouped", load().lb_gemm_trit_planes_grouped(
         arr, len(mats), _ptr(q), _ptr(x_scale), int(M), int(K), _ptr(workspace),
         int(workspace_bytes), _stream(stream)))
+
+
+def lb_dequantize_q1_0(bits, scales, N: int, K: int, out_format: int, out, stream=None):
+    """Every Q1_0 weight as (float)w * d: out [N][K] fp32 (OUT_F32) or bf16 bits (OUT_BF16)."""
+    _check("lb_dequantize_q1_0", load().lb_dequantize_q1_0(
+        _ptr(bits), _ptr(scales), int(N), int(K), int(out_format), _ptr(out), _stream(stream)))
+
+
+def lb_dequantize_q2_0_g64(codes, scales, N: int, K: int, out_format: int, out, stream=None):
+    _check("lb_dequantize_q2_0_g64", load().lb_dequantize_q2_0_g64(
+        _ptr(codes), _ptr(scales), int(N), int(K), int(out_format), _ptr(out), _stream(stream)))
+
+
+def lb_dequantize_trit_planes(planes, w_scale: float, N: int, K: int, out_format: int, out,
+                              stream=None):
+    _check("lb_dequantize_trit_planes", load().lb_dequantize_trit_planes(
+        _ptr(planes), float(w_scale), int(N), int(K), int(out_format), _ptr(out),
+        _stream(stream)))

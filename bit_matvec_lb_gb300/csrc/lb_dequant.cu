@@ -1,0 +1,116 @@
+// lb_dequant.cu -- dequantization of packed weights: every weight as the binary32 product
+// (float)w * d, stored as fp32 or rounded to bf16.
+//
+// "bankml: verified low-bit inference on commodity CPUs -- a technical report": III.4 and IV.2
+// (every weight of every tensor dequantizes bit-identically to the reference's floats), III.2
+// (Q1_0: w = +1 for a set bit, -1 otherwise), III.5 (Q2_0_g64: w = code - 1).  Planar weights
+// (tritium.technology "Architecture", section 2) dequantize to w * w_scale, w in {+1, -1, 0}.
+//
+// HBM-bound streaming kernel: a group of 8 threads takes one 32-column group of one row (the
+// packed word is read once per group and broadcast), each thread writes 4 consecutive outputs,
+// so every warp stores 512 contiguous bytes (fp32) or 256 (bf16).
+#include <cuda_bf16.h>
+
+#include "lb_common.cuh"
+
+namespace lb {
+
+enum DqFmt { kDqQ1 = 0, kDqQ2 = 1, kDqTrit = 2 };
+
+template <int F, bool BF16>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w,
+                                                      const uint16_t *__restrict__ scales,
+                                                      float w_scale, void *__restrict__ out,
+                                                      int64_t N, int64_t K, int S) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t ng = K / 32;
+    const int64_t total = N * ng * 8;  // 8 threads per 32-column group
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += stride) {
+        const int64_t grp = t >> 3;
+        const int part = (int)(t & 7);  // columns 4 part .. 4 part + 3 of the group
+        const int64_t n = grp / ng, g = grp % ng;
+        float v[4];
+        if (F == kDqQ1) {
+            // block g / 4 of the row: 16 sign bytes; this group is its 4-byte word g % 4
+            const uint32_t bits = *reinterpret_cast<const uint32_t *>(w + n * (K / 8) + g * 4);
+            const float d = f16_bits_to_float(scales[n * S + g / 4]);
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                v[j] = (float)(((bits >> (4 * part + j)) & 1u) ? 1 : -1) * d;
+        } else if (F == kDqQ2) {
+            // block g / 2 of the row: 16 code bytes; this group is its 8-byte half g % 2
+            const uint2 c = *reinterpret_cast<const uint2 *>(w + n * (K / 4) + g * 8);
+            const float d = f16_bits_to_float(scales[n * S + g / 2]);
+            const uint32_t word = part < 4 ? c.x : c.y;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int code = (int)((word >> (2 * (4 * (part & 3) + j))) & 3u);
+                v[j] = (float)(code - 1) * d;
+            }
+        } else {
+            // beat g / 2 of the row: {pos lo, pos hi, neg lo, neg hi}; this group is half g % 2
+            const uint4 b = *reinterpret_cast<const uint4 *>(w + (n * (K / 64) + g / 2) * 16);
+            const uint32_t P = (g & 1) ? b.y : b.x, Nn = (g & 1) ? b.w : b.z;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int c = 4 * part + j;
+                const int wt = (int)((P >> c) & 1u) - (int)((Nn >> c) & 1u);
+                v[j] = (float)wt * w_scale;
+            }
+        }
+        const int64_t o = n * K + g * 32 + 4 * part;
+        if (BF16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + o) =
+                make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+        } else {
+            *reinterpret_cast<float4 *>(static_cast<float *>(out) + o) =
+                make_float4(v[0], v[1], v[2], v[3]);
+        }
+    }
+}
+
+template <int F>
+static int dequant(const void *w, const uint16_t *scales, float w_scale, int64_t N, int64_t K,
+                   int out_format, void *out, void *stream) {
+    const int64_t qk = F == kDqQ1 ? 128 : 64;
+    if (!w || !out || (F != kDqTrit && !scales)) return LB_ERR_NULL;
+    if (!aligned16(w) || !aligned16(out) || (scales && !aligned16(scales))) return LB_ERR_ALIGN;
+    if (N < 1 || N > (1ll << 30) || K < qk || K % qk != 0 || K > (1ll << 30)) return LB_ERR_SHAPE;
+    if (out_format != LB_OUT_F32 && out_format != LB_OUT_BF16) return LB_ERR_SHAPE;
+    DeviceInfo di;
+    if (int st = current_device_info(&di)) return st;
+    const int64_t total = N * (K / 32) * 8;
+    int64_t grid = (total + 255) / 256;
+    if (grid > (int64_t)di.sms * 16) grid = (int64_t)di.sms * 16;
+    const int S = (int)((K / qk + 7) / 8 * 8);
+    const uint8_t *wb = static_cast<const uint8_t *>(w);
+    cudaStream_t st = as_stream(stream);
+    if (out_format == LB_OUT_BF16)
+        return launch_pdl(dequant_kernel<F, true>, dim3((unsigned)grid), dim3(256), 0, st, wb,
+                          scales, w_scale, out, N, K, S);
+    return launch_pdl(dequant_kernel<F, false>, dim3((unsigned)grid), dim3(256), 0, st, wb,
+                      scales, w_scale, out, N, K, S);
+}
+
+}  // namespace lb
+
+using namespace lb;
+
+LB_EXPORT int lb_dequantize_q1_0(const uint8_t *bits, const uint16_t *scales, int64_t N,
+                                 int64_t K, int out_format, void *out, void *stream) {
+    return dequant<kDqQ1>(bits, scales, 0.f, N, K, out_format, out, stream);
+}
+
+LB_EXPORT int lb_dequantize_q2_0_g64(const uint8_t *codes, const uint16_t *scales, int64_t N,
+                                     int64_t K, int out_format, void *out, void *stream) {
+    return dequant<kDqQ2>(codes, scales, 0.f, N, K, out_format, out, stream);
+}
+
+LB_EXPORT int lb_dequantize_trit_planes(const uint64_t *planes, float w_scale, int64_t N,
+                                        int64_t K, int out_format, void *out, void *stream) {
+    return dequant<kDqTrit>(planes, nullptr, w_scale, N, K, out_format, out, stream);
+}

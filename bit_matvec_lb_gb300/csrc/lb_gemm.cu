@@ -627,41 +627,48 @@ __device__ __forceinline__ void expand_trit(uint32_t P, uint32_t Nn, uint4 (&c)[
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
-// Four consecutive floats of CTA `rank`'s shared memory at the address this CTA uses for them.
-__device__ __forceinline__ float4 ld_cluster_f4(const float *local, uint32_t rank) {
+// Sixteen consecutive floats (16-byte aligned) of CTA `rank`'s shared memory, at the address
+// this CTA uses for them: four loads issued back to back.  Ordered after the cluster barrier
+// as a volatile statement; no memory clobber, so the loads of several ranks can be in flight
+// together.
+__device__ __forceinline__ void ld_cluster16(const float *local, uint32_t rank, float (&o)[16]) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)),
                  "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote)
-                 : "memory");
-    return v;
+    asm volatile(
+        "ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%16];\n\t"
+        "ld.shared::cluster.v4.f32 {%4, %5, %6, %7}, [%16 + 16];\n\t"
+        "ld.shared::cluster.v4.f32 {%8, %9, %10, %11}, [%16 + 32];\n\t"
+        "ld.shared::cluster.v4.f32 {%12, %13, %14, %15}, [%16 + 48];"
+        : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3]), "=f"(o[4]), "=f"(o[5]), "=f"(o[6]),
+          "=f"(o[7]), "=f"(o[8]), "=f"(o[9]), "=f"(o[10]), "=f"(o[11]), "=f"(o[12]),
+          "=f"(o[13]), "=f"(o[14]), "=f"(o[15])
+        : "r"(remote));
 }
 
-// The 32 outputs of token row m (yrow / arow point at its row) for weight rows nb .. nb + 31,
+// The W outputs of token row m (yrow / arow point at its row) for weight rows nb .. nb + W - 1,
 // from their exact integer accumulators a[].
-__device__ __forceinline__ void trit_store32(const float (&a)[32], float xs, float w_scale,
-                                             float *yrow, int32_t *arow, int64_t nb, int N) {
-    float o[32];
+template <int W>
+__device__ __forceinline__ void trit_store(const float (&a)[W], float xs, float w_scale,
+                                           float *yrow, int32_t *arow, int64_t nb, int N) {
+    float o[W];
 #pragma unroll
-    for (int j = 0; j < 32; j++) o[j] = __fmul_rn(__fmul_rn(a[j], xs), w_scale);
-    if ((N & 3) == 0 && nb + 32 <= N) {
+    for (int j = 0; j < W; j++) o[j] = __fmul_rn(__fmul_rn(a[j], xs), w_scale);
+    if ((N & 3) == 0 && nb + W <= N) {
 #pragma unroll
-        for (int v = 0; v < 8; v++)
+        for (int v = 0; v < W / 4; v++)
             reinterpret_cast<float4 *>(yrow + nb)[v] =
                 make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         if (arow) {
 #pragma unroll
-            for (int v = 0; v < 8; v++)
+            for (int v = 0; v < W / 4; v++)
                 reinterpret_cast<int4 *>(arow + nb)[v] = make_int4(
                     __float2int_rn(a[4 * v]), __float2int_rn(a[4 * v + 1]),
                     __float2int_rn(a[4 * v + 2]), __float2int_rn(a[4 * v + 3]));
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; j++) {
+        for (int j = 0; j < W; j++) {
             if (nb + j < N) {
                 yrow[nb + j] = o[j];
                 if (arow) arow[nb + j] = __float2int_rn(a[j]);
@@ -783,7 +790,7 @@ __global__ void __launch_bounds__(kTritThreads, 2)
                 float a[32];
 #pragma unroll
                 for (int j = 0; j < 32; j++) a[j] = __uint_as_float(r[j]);
-                trit_store32(a, xs, W.w_scale, yrow, arow, n0 + 32 * c, W.N);
+                trit_store<32>(a, xs, W.w_scale, yrow, arow, n0 + 32 * c, W.N);
             }
         }
     } else if (warp == 4) {
@@ -833,31 +840,31 @@ __global__ void __launch_bounds__(kTritThreads, 2)
 
     if (p.ks > 1) {
         // Split tiles: every CTA of the cluster has parked its partial tile (every thread of
-        // every CTA arrives here once, whatever its role).  CTA `split` then adds the column
-        // chunks c = split, split + ks, ... over the cluster and writes their outputs; the second
-        // barrier keeps every partial alive until all CTAs have read it.
+        // every CTA arrives here once, whatever its role).  CTA `split` then adds the 16-column
+        // chunks c = split, split + ks, ... over the cluster (the loads of all ranks in flight
+        // together) and writes their outputs; the second barrier keeps every partial alive until
+        // all CTAs have read it.
         __syncwarp();
         cluster_sync_all();
         if (warp < 4) {
             float *yrow = W.y + (mvalid ? m : 0) * (int64_t)W.N;
             int32_t *arow = W.acc ? W.acc + (mvalid ? m : 0) * (int64_t)W.N : nullptr;
-            for (int c = split; c < kTileN / 32; c += p.ks) {
-                float a[32];
+            for (int c = split; c < kTileN / 16; c += p.ks) {
+                const float *src = part + mrow * kPartPitch + 16 * c;
+                float t[kTritMaxSplit][16];
 #pragma unroll
-                for (int j = 0; j < 32; j++) a[j] = 0.f;
-                const float *src = part + mrow * kPartPitch + 32 * c;
+                for (int s = 0; s < kTritMaxSplit; s++)
+                    if (s < p.ks) ld_cluster16(src, (uint32_t)s, t[s]);
                 // integer partials: every sum stays an integer below 2^24, exact in any order
-                for (int s = 0; s < p.ks; s++) {
+                float a[16];
 #pragma unroll
-                    for (int v = 0; v < 8; v++) {
-                        const float4 t = ld_cluster_f4(src + 4 * v, (uint32_t)s);
-                        a[4 * v] += t.x;
-                        a[4 * v + 1] += t.y;
-                        a[4 * v + 2] += t.z;
-                        a[4 * v + 3] += t.w;
-                    }
+                for (int j = 0; j < 16; j++) {
+                    a[j] = t[0][j];
+#pragma unroll
+                    for (int s = 1; s < kTritMaxSplit; s++)
+                        if (s < p.ks) a[j] += t[s][j];
                 }
-                if (mvalid) trit_store32(a, xs, W.w_scale, yrow, arow, n0 + 32 * c, W.N);
+                if (mvalid) trit_store<16>(a, xs, W.w_scale, yrow, arow, n0 + 16 * c, W.N);
             }
         }
         __syncwarp();

@@ -284,6 +284,28 @@ int lb_gemm_trit_planes_grouped(const lb_trit_matrix *mats, int G, const int8_t 
                                 const float *x_scale, int64_t M, int64_t K, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Dequantization ([TR] III.4 and IV.2: every weight of a tensor dequantized and compared with
+ * the reference's floats; III.2 and III.5 define w).  Every weight as the binary32 product
+ *   out[n][k] = (float)w[n][k] * d      (exact: w in {-1, +1} or {-1, 0, +1, +2})
+ * with d the fp16 block scale widened to binary32 (Q1_0, Q2_0_g64, from the repacked planes)
+ * or w_scale (planar, w in {-1, 0, +1}).  A zero weight gives +0 or -0 with the sign of d.
+ *   out_format LB_OUT_F32  : out [N][K] fp32.
+ *   out_format LB_OUT_BF16 : out [N][K] bf16 bit patterns, the binary32 value rounded to
+ *                            nearest, ties to even (the pages print no bf16 weights; this is
+ *                            the plainest reading).
+ * Q1_0: K % 128 == 0; Q2_0_g64 and planar: K % 64 == 0; 1 <= N <= 2^30, K <= 2^30.
+ * Errors: LB_ERR_NULL, LB_ERR_ALIGN, LB_ERR_SHAPE (also an unknown out_format), LB_ERR_ARCH,
+ * LB_ERR_LAUNCH. */
+#define LB_OUT_F32 0
+#define LB_OUT_BF16 1
+int lb_dequantize_q1_0(const uint8_t *bits, const uint16_t *scales, int64_t N, int64_t K,
+                       int out_format, void *out, void *stream);
+int lb_dequantize_q2_0_g64(const uint8_t *codes, const uint16_t *scales, int64_t N, int64_t K,
+                           int out_format, void *out, void *stream);
+int lb_dequantize_trit_planes(const uint64_t *planes, float w_scale, int64_t N, int64_t K,
+                              int out_format, void *out, void *stream);
+
 /* ---- Q2_0_g64 prefill GEMM without caller scratch.
  * No counterpart in the source pages: a convenience of this library for callers that cannot
  * allocate device memory.  Same arithmetic, accuracy, layouts and errors as lb_gemm_q2_0_g64,

@@ -69,6 +69,9 @@ def _load():
                 "oracle_bf16_product": (None, [P, P, I64, I64, I64, P, P]),
                 "oracle_repack": (None, [P, I64, I64, P, P]),
                 "oracle_dequant": (None, [ctypes.c_int, P, I64, I64, P]),
+                "oracle_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+                "oracle_f32_to_bf16_array": (None, [P, I64, P]),
+                "oracle_trit_planes_dequant": (ctypes.c_int, [P, ctypes.c_float, I64, I64, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -245,4 +248,30 @@ def dequant(blocks: np.ndarray, K: int, qk: int) -> np.ndarray:
     N = blocks.shape[0]
     out = np.empty((N, K), dtype=np.float32)
     _load().oracle_dequant(qk, _ptr(blocks), N, K, _ptr(out))
+    return out
+
+
+def f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    """binary32 -> bf16 bit patterns, round to nearest, ties to even (reading R10)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_f32_to_bf16_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def dequant_bf16(blocks: np.ndarray, K: int, qk: int) -> np.ndarray:
+    """Every weight as bf16 bits of the binary32 w * d, [N][K] (reading R10)."""
+    return f32_to_bf16(dequant(blocks, K, qk))
+
+
+def trit_planes_dequant(planes: np.ndarray, w_scale: float, K: int) -> np.ndarray:
+    """Planar weights as float32 w * w_scale, [N][K] (readings R5, R10); raises on an
+    overlapping beat."""
+    planes = np.ascontiguousarray(planes, dtype=np.uint64)
+    N = planes.shape[0]
+    assert planes.size == N * (K // 64) * 2
+    out = np.empty((N, K), dtype=np.float32)
+    if _load().oracle_trit_planes_dequant(_ptr(planes), float(np.float32(w_scale)), N, K,
+                                          _ptr(out)) == -1:
+        raise ValueError("planar beat with a column in both the pos and neg planes")
     return out

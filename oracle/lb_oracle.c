@@ -30,6 +30,11 @@
  *   R8  bf16 head: weight widened by a 16-bit left shift, activations fp32,
  *       y = sum_k w*x ([TA] section 3: the dense head is stored bf16 and run in f32).
  *   R9  y is token-major [B][N]; W is row-major [N][K] (rows are outputs).
+ *   R10 Dequantization gives every weight as the binary32 product (float)w * d
+ *       ([TR] III.4 and IV.2 compare every dequantized weight with the reference's
+ *       floats); a bf16 copy is that binary32 value rounded to nearest, ties to even
+ *       (the pages print no bf16 weights).  Planar weights dequantize to
+ *       (float)w * w_scale with w = +1 / -1 / 0 ([TA] sections 2 and 5).
  *
  * Outputs of the Q1_0 / Q2_0_g64 products are produced three ways: the integer
  * block sums isum (exact), the exact value E in double, and the magnitude
@@ -399,4 +404,58 @@ ORACLE_API void oracle_dequant(int qk, const uint8_t *blocks, int64_t N, int64_t
             }
         }
     }
+}
+
+/* ------------------------------------------------------------------------- */
+/* binary32 -> bf16, round to nearest, ties to even (reading R10), from the    */
+/* IEEE 754 layout: bf16 keeps the sign, the 8 exponent bits and the top 7     */
+/* fraction bits of a binary32.  The 16 dropped bits decide the rounding: more */
+/* than half an ulp rounds the magnitude up, exactly half rounds to the even   */
+/* neighbour (a carry out of the fraction correctly bumps the exponent, up to  */
+/* infinity).  NaN stays NaN (quiet bit set); infinities are exact.            */
+/* ------------------------------------------------------------------------- */
+ORACLE_API uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t u = f32_bits(f);
+    uint32_t keep = u >> 16;
+    uint32_t drop = u & 0xFFFFu;
+    if ((u & 0x7F800000u) == 0x7F800000u)          /* Inf or NaN */
+        return (uint16_t)(drop ? (keep | 0x0040u) : keep);
+    if (drop > 0x8000u || (drop == 0x8000u && (keep & 1u)))
+        keep += 1u;
+    return (uint16_t)keep;
+}
+
+ORACLE_API void oracle_f32_to_bf16_array(const float *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = oracle_f32_to_bf16(x[i]);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Planar dequantization (readings R5, R10): out[r][64g + c] = (float)w *       */
+/* w_scale with w = +1 (pos bit), -1 (neg bit), 0 (neither).  Returns 0, or -1 */
+/* if some beat has a column in both planes.                                   */
+/* ------------------------------------------------------------------------- */
+ORACLE_API int oracle_trit_planes_dequant(const uint64_t *planes, float w_scale, int64_t N,
+                                          int64_t K, float *out)
+{
+    int64_t nbeat = K / 64;
+    for (int64_t r = 0; r < N; r++) {
+        for (int64_t g = 0; g < nbeat; g++) {
+            uint64_t pos = planes[(r * nbeat + g) * 2 + 0];
+            uint64_t neg = planes[(r * nbeat + g) * 2 + 1];
+            if (pos & neg)
+                return -1;
+            for (int c = 0; c < 64; c++) {
+                int w = 0;
+                if ((pos >> c) & 1u)
+                    w = 1;
+                else if ((neg >> c) & 1u)
+                    w = -1;
+                out[r * K + g * 64 + c] = (float)w * w_scale;
+            }
+        }
+    }
+    return 0;
 }

@@ -240,3 +240,26 @@ def test_gemm_trit_refusals(lib):
     assert g(arr, 2, A, A, 16, K, A, ws, None) == -2      # misaligned acc of matrix 1
     arr[1] = lb.lb_trit_matrix(A, 1.0, A, None, 0)
     assert g(arr, 2, A, A, 16, K, A, ws, None) == -3      # N = 0
+
+
+# ---- dequantization: host checks ----
+@pytest.mark.parametrize("fn,qk", [("lb_dequantize_q1_0", 128), ("lb_dequantize_q2_0_g64", 64)])
+def test_dequant_refusals(lib, fn, qk):
+    f = getattr(lib, fn)
+    assert f(None, A, 4, qk, 0, A, None) == -1
+    assert f(A, None, 4, qk, 0, A, None) == -1
+    assert f(A, A, 4, qk, 0, None, None) == -1
+    assert f(MIS, A, 4, qk, 0, A, None) == -2
+    assert f(A, A, 4, qk, 1, MIS, None) == -2
+    assert f(A, A, 4, qk // 2, 0, A, None) == -3
+    assert f(A, A, 0, qk, 0, A, None) == -3
+    assert f(A, A, 4, qk, 2, A, None) == -3      # unknown output format
+    assert f(A, A, 4, qk, -1, A, None) == -3
+
+
+def test_dequant_trit_refusals(lib):
+    f = lib.lb_dequantize_trit_planes
+    assert f(None, 1.0, 4, 64, 0, A, None) == -1
+    assert f(A, 1.0, 4, 64, 0, MIS, None) == -2
+    assert f(A, 1.0, 4, 96, 0, A, None) == -3
+    assert f(A, 1.0, 4, 64, 3, A, None) == -3

@@ -389,3 +389,67 @@ def test_dequant_matches_independent_decode():
     d2 = oracle.dequant(b2, K, 64)
     assert np.array_equal(d1, (_q1_dense(b1, K) * np.repeat(_f16(_scales(b1)), 128, 1)).astype(np.float32))
     assert np.array_equal(d2, (_q2_dense(b2, K) * np.repeat(_f16(_scales(b2)), 64, 1)).astype(np.float32))
+
+
+# ----------------------------------------------------------------------------------------------
+# dequantization to bf16 and planar dequantization (reading R10)
+# ----------------------------------------------------------------------------------------------
+def _torch_bf16_bits(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+def test_f32_to_bf16_against_torch():
+    """Round to nearest, ties to even, pinned against torch's own float32 -> bfloat16 conversion
+    (an independent implementation): every dequantized value a weight can take (every finite
+    fp16 scale times -1, +1 and +2), constructed ties with even and odd kept halves, and random
+    binary32 bit patterns."""
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = h.view(np.float16).astype(np.float32)
+    f = f[np.isfinite(f)]
+    vals = [f, -f, 2 * f]
+    keep = np.arange(0, 1 << 16, 7, dtype=np.uint32)
+    keep = keep[(keep & 0x7F80) != 0x7F80]          # finite kept halves
+    for drop in (0x8000, 0x7FFF, 0x8001, 0x0000, 0xFFFF):
+        vals.append(((keep << 16) | drop).view(np.float32))
+    g = synth.rng(99)
+    r = g.integers(0, 1 << 32, size=1 << 20, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    vals.append(r[np.isfinite(r)])
+    x = np.concatenate(vals)
+    assert np.array_equal(oracle.f32_to_bf16(x), _torch_bf16_bits(x))
+    # infinities stay infinite, NaN stays NaN
+    special = np.array([np.inf, -np.inf, np.nan], np.float32)
+    out = oracle.f32_to_bf16(special)
+    assert out[0] == 0x7F80 and out[1] == 0xFF80 and (out[2] & 0x7F80) == 0x7F80 and out[2] & 0x7F
+
+
+def test_f32_to_bf16_ties_by_hand():
+    # 1 + 2^-8 is half an ulp above 1.0 (bf16 keeps 7 fraction bits): ties go to the even 1.0;
+    # 1 + 3 * 2^-8 is half-way between 1 + 2^-7 (odd) and 1 + 2^-6 (even): rounds up
+    assert oracle.f32_to_bf16(np.array([1.00390625, 1.01171875, -1.00390625], np.float32)).tolist() \
+        == [0x3F80, 0x3F82, 0xBF80]
+
+
+def test_dequant_bf16_is_rounded_f32():
+    N, K = 4, 512
+    b = synth.q2_0_blocks(N, K, seed=83, probs=(0.25, 0.25, 0.25, 0.25))
+    f = oracle.dequant(b, K, 64)
+    assert np.array_equal(oracle.dequant_bf16(b, K, 64), _torch_bf16_bits(f))
+
+
+def test_trit_planes_dequant_matches_generator_trits():
+    """The oracle's decode of the planes against the dense trits the encoder was given."""
+    N, K = 5, 320
+    planes, trits = synth.trit_planes(N, K, seed=84)
+    w = synth.w_scale(85)
+    assert np.array_equal(oracle.trit_planes_dequant(planes, w, K),
+                          trits.astype(np.float32) * np.float32(w))
+    neg = -0.5
+    d = oracle.trit_planes_dequant(planes, neg, K)
+    assert np.array_equal(np.signbit(d[trits == 0]), np.ones((trits == 0).sum(), bool))
+    bad = planes.copy()
+    bad[0, 0, 1] |= bad[0, 0, 0] | np.uint64(1)
+    bad[0, 0, 0] |= np.uint64(1)
+    with pytest.raises(ValueError):
+        oracle.trit_planes_dequant(bad, w, K)
