@@ -443,8 +443,8 @@ ORACLE_API int oracle_trit_planes_dequant(const uint64_t *planes, float w_scale,
     int64_t nbeat = K / 64;
     for (int64_t r = 0; r < N; r++) {
         for (int64_t g = 0; g < nbeat; g++) {
-            uint64_t pos = planes[(r * nbeat + g) * 2 + 0];
-            uint64_t neg = planes[(r * nbeat + g) * 2 + 1];
+            const uint64_t *beat = planes + (r * nbeat + g) * 2;   /* {pos, neg} */
+            uint64_t pos = beat[0], neg = beat[1];
             if (pos & neg)
                 return -1;
             for (int c = 0; c < 64; c++) {

@@ -44,6 +44,11 @@ MUTANTS = [
      "return (uint16_t)(block18[0] | ((uint16_t)block18[1] << 8));",
      "return (uint16_t)(block18[1] | ((uint16_t)block18[0] << 8));"),
     ("bf16_wrong_shift", "return bits_f32((uint32_t)b << 16);", "return bits_f32((uint32_t)b << 15);"),
+    ("bf16_round_truncates", "if (drop > 0x8000u || (drop == 0x8000u && (keep & 1u)))",
+     "if (0)"),
+    ("bf16_ties_away", "(drop == 0x8000u && (keep & 1u))", "(drop == 0x8000u)"),
+    ("planar_dequant_swapped_planes", "uint64_t pos = beat[0], neg = beat[1];",
+     "uint64_t pos = beat[1], neg = beat[0];"),
 ]
 
 
