@@ -8,7 +8,8 @@
 //
 // HBM-bound streaming kernel: a group of 8 threads takes one 32-column group of one row (the
 // packed word is read once per group and broadcast), each thread writes 4 consecutive outputs,
-// so every warp stores 512 contiguous bytes (fp32) or 256 (bf16).
+// so every warp stores 512 contiguous bytes (fp32) or 256 (bf16); every thread keeps several
+// groups' loads in flight.
 #include <cuda_bf16.h>
 
 #include "lb_common.cuh"
@@ -16,6 +17,57 @@
 namespace lb {
 
 enum DqFmt { kDqQ1 = 0, kDqQ2 = 1, kDqTrit = 2 };
+
+// The packed word of (row n, 32-column group g) and its scale.
+template <int F>
+struct DqIn {
+    uint4 w;
+    float d;
+};
+
+template <int F>
+__device__ __forceinline__ DqIn<F> dq_load(const uint8_t *__restrict__ w,
+                                           const uint16_t *__restrict__ scales, float w_scale,
+                                           int64_t n, int64_t g, int64_t K, int S) {
+    DqIn<F> r;
+    if (F == kDqQ1) {
+        // block g / 4 of the row: 16 sign bytes; this group is its 4-byte word g % 4
+        r.w = make_uint4(*reinterpret_cast<const uint32_t *>(w + n * (K / 8) + g * 4), 0, 0, 0);
+        r.d = f16_bits_to_float(scales[n * S + g / 4]);
+    } else if (F == kDqQ2) {
+        // block g / 2 of the row: 16 code bytes; this group is its 8-byte half g % 2
+        const uint2 c = *reinterpret_cast<const uint2 *>(w + n * (K / 4) + g * 8);
+        r.w = make_uint4(c.x, c.y, 0, 0);
+        r.d = f16_bits_to_float(scales[n * S + g / 2]);
+    } else {
+        // beat g / 2 of the row: {pos lo, pos hi, neg lo, neg hi}; this group is half g % 2
+        const uint4 b = *reinterpret_cast<const uint4 *>(w + (n * (K / 64) + g / 2) * 16);
+        r.w = (g & 1) ? make_uint4(b.y, b.w, 0, 0) : make_uint4(b.x, b.z, 0, 0);
+        r.d = w_scale;
+    }
+    return r;
+}
+
+// Columns 4 part .. 4 part + 3 of the group as (float)w * d.
+template <int F>
+__device__ __forceinline__ void dq_values(const DqIn<F> &in, int part, float (&v)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int c = 4 * part + j;
+        int wt;
+        if (F == kDqQ1)
+            wt = ((in.w.x >> c) & 1u) ? 1 : -1;
+        else if (F == kDqQ2)
+            wt = (int)(((c < 16 ? in.w.x : in.w.y) >> (2 * (c & 15))) & 3u) - 1;
+        else
+            wt = (int)((in.w.x >> c) & 1u) - (int)((in.w.y >> c) & 1u);
+        v[j] = (float)wt * in.d;
+    }
+}
+
+// Thread t of 8 per group writes columns 4 (t % 8) .. + 3; each thread takes kU groups per
+// iteration, their loads issued before any conversion (kU independent loads in flight).
+constexpr int kU = 4;
 
 template <int F, bool BF16>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w,
@@ -27,48 +79,35 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
     const int64_t ng = K / 32;
     const int64_t total = N * ng * 8;  // 8 threads per 32-column group
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += stride) {
-        const int64_t grp = t >> 3;
-        const int part = (int)(t & 7);  // columns 4 part .. 4 part + 3 of the group
-        const int64_t n = grp / ng, g = grp % ng;
-        float v[4];
-        if (F == kDqQ1) {
-            // block g / 4 of the row: 16 sign bytes; this group is its 4-byte word g % 4
-            const uint32_t bits = *reinterpret_cast<const uint32_t *>(w + n * (K / 8) + g * 4);
-            const float d = f16_bits_to_float(scales[n * S + g / 4]);
+    for (int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t0 < total;
+         t0 += kU * stride) {
+        DqIn<F> in[kU];
 #pragma unroll
-            for (int j = 0; j < 4; j++)
-                v[j] = (float)(((bits >> (4 * part + j)) & 1u) ? 1 : -1) * d;
-        } else if (F == kDqQ2) {
-            // block g / 2 of the row: 16 code bytes; this group is its 8-byte half g % 2
-            const uint2 c = *reinterpret_cast<const uint2 *>(w + n * (K / 4) + g * 8);
-            const float d = f16_bits_to_float(scales[n * S + g / 2]);
-            const uint32_t word = part < 4 ? c.x : c.y;
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int code = (int)((word >> (2 * (4 * (part & 3) + j))) & 3u);
-                v[j] = (float)(code - 1) * d;
-            }
-        } else {
-            // beat g / 2 of the row: {pos lo, pos hi, neg lo, neg hi}; this group is half g % 2
-            const uint4 b = *reinterpret_cast<const uint4 *>(w + (n * (K / 64) + g / 2) * 16);
-            const uint32_t P = (g & 1) ? b.y : b.x, Nn = (g & 1) ? b.w : b.z;
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const int c = 4 * part + j;
-                const int wt = (int)((P >> c) & 1u) - (int)((Nn >> c) & 1u);
-                v[j] = (float)wt * w_scale;
+        for (int u = 0; u < kU; u++) {
+            const int64_t t = t0 + u * stride;
+            if (t < total) {
+                const int64_t grp = t >> 3;
+                in[u] = dq_load<F>(w, scales, w_scale, grp / ng, grp % ng, K, S);
             }
         }
-        const int64_t o = n * K + g * 32 + 4 * part;
-        if (BF16) {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
-            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + o) =
-                make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-        } else {
-            *reinterpret_cast<float4 *>(static_cast<float *>(out) + o) =
-                make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+            const int64_t t = t0 + u * stride;
+            if (t >= total) break;
+            const int64_t grp = t >> 3;
+            const int part = (int)(t & 7);
+            float v[4];
+            dq_values<F>(in[u], part, v);
+            const int64_t o = (grp / ng) * K + (grp % ng) * 32 + 4 * part;
+            if (BF16) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + o) = make_uint2(
+                    *reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            } else {
+                *reinterpret_cast<float4 *>(static_cast<float *>(out) + o) =
+                    make_float4(v[0], v[1], v[2], v[3]);
+            }
         }
     }
 }
@@ -84,7 +123,7 @@ static int dequant(const void *w, const uint16_t *scales, float w_scale, int64_t
     DeviceInfo di;
     if (int st = current_device_info(&di)) return st;
     const int64_t total = N * (K / 32) * 8;
-    int64_t grid = (total + 255) / 256;
+    int64_t grid = (total + 256 * kU - 1) / (256 * kU);
     if (grid > (int64_t)di.sms * 16) grid = (int64_t)di.sms * 16;
     const int S = (int)((K / qk + 7) / 8 * 8);
     const uint8_t *wb = static_cast<const uint8_t *>(w);
