@@ -9,8 +9,10 @@
 // HBM-bound streaming kernel: a group of 8 threads takes one 32-column group of one row (the
 // packed word is read once per group and broadcast), each thread writes 4 consecutive outputs,
 // so every warp stores 512 contiguous bytes (fp32) or 256 (bf16); every thread keeps several
-// groups' loads in flight.
+// groups' loads in flight.  Blocks take whole rows, so indices need no division.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "lb_common.cuh"
 
@@ -65,8 +67,9 @@ __device__ __forceinline__ void dq_values(const DqIn<F> &in, int part, float (&v
     }
 }
 
-// Thread t of 8 per group writes columns 4 (t % 8) .. + 3; each thread takes kU groups per
-// iteration, their loads issued before any conversion (kU independent loads in flight).
+// A block takes whole rows (rows blockIdx.x, blockIdx.x + gridDim.x, ...).  Within a row, slot t
+// = 8 g + part writes columns 4 part .. 4 part + 3 of group g, so no index needs a division;
+// each thread takes kU slots per iteration, their loads issued before any conversion.
 constexpr int kU = 4;
 
 template <int F, bool BF16>
@@ -76,37 +79,31 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
                                                       int64_t N, int64_t K, int S) {
     pdl_launch_dependents();
     pdl_wait();
-    const int64_t ng = K / 32;
-    const int64_t total = N * ng * 8;  // 8 threads per 32-column group
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t0 < total;
-         t0 += kU * stride) {
-        DqIn<F> in[kU];
+    const int slots = (int)(K / 32) * 8;  // 8 threads per 32-column group
+    for (int64_t n = blockIdx.x; n < N; n += gridDim.x) {
+        for (int t0 = threadIdx.x; t0 < slots; t0 += kU * blockDim.x) {
+            DqIn<F> in[kU];
 #pragma unroll
-        for (int u = 0; u < kU; u++) {
-            const int64_t t = t0 + u * stride;
-            if (t < total) {
-                const int64_t grp = t >> 3;
-                in[u] = dq_load<F>(w, scales, w_scale, grp / ng, grp % ng, K, S);
+            for (int u = 0; u < kU; u++) {
+                const int t = t0 + u * (int)blockDim.x;
+                if (t < slots) in[u] = dq_load<F>(w, scales, w_scale, n, t >> 3, K, S);
             }
-        }
 #pragma unroll
-        for (int u = 0; u < kU; u++) {
-            const int64_t t = t0 + u * stride;
-            if (t >= total) break;
-            const int64_t grp = t >> 3;
-            const int part = (int)(t & 7);
-            float v[4];
-            dq_values<F>(in[u], part, v);
-            const int64_t o = (grp / ng) * K + (grp % ng) * 32 + 4 * part;
-            if (BF16) {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
-                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + o) = make_uint2(
-                    *reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-            } else {
-                *reinterpret_cast<float4 *>(static_cast<float *>(out) + o) =
-                    make_float4(v[0], v[1], v[2], v[3]);
+            for (int u = 0; u < kU; u++) {
+                const int t = t0 + u * (int)blockDim.x;
+                if (t >= slots) break;
+                float v[4];
+                dq_values<F>(in[u], t & 7, v);
+                const int64_t o = n * K + (int64_t)(t >> 3) * 32 + 4 * (t & 7);
+                if (BF16) {
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+                    __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+                    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + o) = make_uint2(
+                        *reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                } else {
+                    *reinterpret_cast<float4 *>(static_cast<float *>(out) + o) =
+                        make_float4(v[0], v[1], v[2], v[3]);
+                }
             }
         }
     }
@@ -118,13 +115,12 @@ static int dequant(const void *w, const uint16_t *scales, float w_scale, int64_t
     const int64_t qk = F == kDqQ1 ? 128 : 64;
     if (!w || !out || (F != kDqTrit && !scales)) return LB_ERR_NULL;
     if (!aligned16(w) || !aligned16(out) || (scales && !aligned16(scales))) return LB_ERR_ALIGN;
-    if (N < 1 || N > (1ll << 30) || K < qk || K % qk != 0 || K > (1ll << 30)) return LB_ERR_SHAPE;
+    if (N < 1 || N > (1ll << 30) || K < qk || K % qk != 0 || K > (1ll << 26)) return LB_ERR_SHAPE;
     if (out_format != LB_OUT_F32 && out_format != LB_OUT_BF16) return LB_ERR_SHAPE;
     DeviceInfo di;
     if (int st = current_device_info(&di)) return st;
-    const int64_t total = N * (K / 32) * 8;
-    int64_t grid = (total + 256 * kU - 1) / (256 * kU);
-    if (grid > (int64_t)di.sms * 16) grid = (int64_t)di.sms * 16;
+    // whole rows per block: enough blocks for 8 resident per SM (fewer for few rows)
+    int64_t grid = std::min<int64_t>(N, (int64_t)di.sms * 8);
     const int S = (int)((K / qk + 7) / 8 * 8);
     const uint8_t *wb = static_cast<const uint8_t *>(w);
     cudaStream_t st = as_stream(stream);

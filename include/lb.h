@@ -294,7 +294,7 @@ int lb_gemm_trit_planes_grouped(const lb_trit_matrix *mats, int G, const int8_t 
  *   out_format LB_OUT_BF16 : out [N][K] bf16 bit patterns, the binary32 value rounded to
  *                            nearest, ties to even (the pages print no bf16 weights; this is
  *                            the plainest reading).
- * Q1_0: K % 128 == 0; Q2_0_g64 and planar: K % 64 == 0; 1 <= N <= 2^30, K <= 2^30.
+ * Q1_0: K % 128 == 0; Q2_0_g64 and planar: K % 64 == 0; 1 <= N <= 2^30, K <= 2^26.
  * Errors: LB_ERR_NULL, LB_ERR_ALIGN, LB_ERR_SHAPE (also an unknown out_format), LB_ERR_ARCH,
  * LB_ERR_LAUNCH. */
 #define LB_OUT_F32 0
