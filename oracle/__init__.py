@@ -72,6 +72,10 @@ def _load():
                 "oracle_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
                 "oracle_f32_to_bf16_array": (None, [P, I64, P]),
                 "oracle_trit_planes_dequant": (ctypes.c_int, [P, ctypes.c_float, I64, I64, P]),
+                "oracle_base3_pack": (ctypes.c_int, [P, I64, I64, P]),
+                "oracle_base3_product": (ctypes.c_int, [P, ctypes.c_float, P, P, I64, I64, I64,
+                                                        P, P]),
+                "oracle_base3_unpack": (None, [P, I64, I64, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -275,3 +279,48 @@ def trit_planes_dequant(planes: np.ndarray, w_scale: float, K: int) -> np.ndarra
                                           _ptr(out)) == -1:
         raise ValueError("planar beat with a column in both the pos and neg planes")
     return out
+
+
+def base3_row_bytes(K: int) -> int:
+    """Bytes per base-3 packed row: ceil(K / 80) groups of 16 bytes (reading R15)."""
+    return (K + 79) // 80 * 16
+
+
+def base3_pack(planes: np.ndarray, K: int) -> np.ndarray:
+    """Planar beats [N][K/64][2] -> base-3 bytes [N][base3_row_bytes(K)] ([TR] III.8, R15)."""
+    planes = np.ascontiguousarray(planes, dtype=np.uint64)
+    N = planes.shape[0]
+    out = np.empty((N, base3_row_bytes(K)), dtype=np.uint8)
+    if _load().oracle_base3_pack(_ptr(planes), N, K, _ptr(out)) == -1:
+        raise ValueError("planar beat with a column in both the pos and neg planes")
+    return out
+
+
+def base3_unpack(packed: np.ndarray, K: int) -> np.ndarray:
+    """Base-3 bytes -> trits int8 [N][K] (R15)."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    N = packed.shape[0]
+    out = np.empty((N, K), dtype=np.int8)
+    _load().oracle_base3_unpack(_ptr(packed), N, K, _ptr(out))
+    return out
+
+
+def base3_product(packed: np.ndarray, w_scale: float, q: np.ndarray, x_scale: np.ndarray):
+    """Base-3 packed ternary x int8 (R6, R7, R15). Returns (acc int32 [B][N], y float32)."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    if q.ndim == 1:
+        q = q[None, :]
+    x_scale = np.ascontiguousarray(np.atleast_1d(x_scale), dtype=np.float32)
+    B, K = q.shape
+    N = packed.shape[0]
+    assert packed.shape[1] == base3_row_bytes(K)
+    acc = np.empty((B, N), dtype=np.int32)
+    y = np.empty((B, N), dtype=np.float32)
+    rc = _load().oracle_base3_product(_ptr(packed), float(np.float32(w_scale)), _ptr(q),
+                                      _ptr(x_scale), N, K, B, _ptr(acc), _ptr(y))
+    if rc == -1:
+        raise ValueError("byte above 242 in a base-3 packed matrix")
+    if rc == -2:
+        raise OverflowError("accumulator outside int32")
+    return acc, y

@@ -35,6 +35,11 @@
  *       floats); a bf16 copy is that binary32 value rounded to nearest, ties to even
  *       (the pages print no bf16 weights).  Planar weights dequantize to
  *       (float)w * w_scale with w = +1 / -1 / 0 ([TA] sections 2 and 5).
+ *   R15 Base-3 packing ([TR] III.8: 3^5 = 243 <= 256, five trits per byte): byte j
+ *       of 16-byte group g of a row holds columns 80g + 5j + i, i = 0..4, as the
+ *       base-3 number sum_i (t + 1) * 3^i (digit i = column 80g + 5j + i, lowest
+ *       column in the lowest digit); a row is ceil(K/80) groups, columns >= K hold
+ *       trit 0.  The product has the planar arithmetic (R6, R7).
  *
  * Outputs of the Q1_0 / Q2_0_g64 products are produced three ways: the integer
  * block sums isum (exact), the exact value E in double, and the magnitude
@@ -458,4 +463,104 @@ ORACLE_API int oracle_trit_planes_dequant(const uint64_t *planes, float w_scale,
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Base-3 packing (reading R15): trits of a row -> bytes, from the planar      */
+/* layout.  out is [N][ceil(K/80) * 16].  Returns 0, or -1 if a planar beat   */
+/* has a column in both planes.                                               */
+/* ------------------------------------------------------------------------- */
+static int planar_trit(const uint64_t *planes, int64_t nbeat, int64_t r, int64_t col)
+{
+    uint64_t pos = planes[(r * nbeat + col / 64) * 2 + 0];
+    uint64_t neg = planes[(r * nbeat + col / 64) * 2 + 1];
+    int bit = (int)(col % 64);
+    if ((pos >> bit) & (neg >> bit) & 1u)
+        return 2;                                   /* invalid: both planes */
+    if ((pos >> bit) & 1u)
+        return 1;
+    if ((neg >> bit) & 1u)
+        return -1;
+    return 0;
+}
+
+ORACLE_API int oracle_base3_pack(const uint64_t *planes, int64_t N, int64_t K, uint8_t *out)
+{
+    int64_t nbeat = K / 64;
+    int64_t ngroup = (K + 79) / 80;
+    for (int64_t r = 0; r < N; r++) {
+        for (int64_t g = 0; g < ngroup; g++) {
+            for (int j = 0; j < 16; j++) {
+                int value = 0, place = 1;
+                for (int i = 0; i < 5; i++) {
+                    int64_t col = 80 * g + 5 * j + i;
+                    int t = col < K ? planar_trit(planes, nbeat, r, col) : 0;
+                    if (t == 2)
+                        return -1;
+                    value += (t + 1) * place;       /* digit i = trit + 1 */
+                    place *= 3;
+                }
+                out[(r * ngroup + g) * 16 + j] = (uint8_t)value;
+            }
+        }
+    }
+    return 0;
+}
+
+/* Trit of column col of a base-3 packed row (reading R15): digit i of byte j  */
+/* of group g, found by dividing by 3 i times.                                 */
+static int base3_trit(const uint8_t *row, int64_t col)
+{
+    int64_t g = col / 80;
+    int j = (int)((col % 80) / 5), i = (int)(col % 5);
+    int value = row[g * 16 + j];
+    for (int k = 0; k < i; k++)
+        value /= 3;
+    return value % 3 - 1;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Base-3 product (readings R6, R7, R15): the planar arithmetic on trits       */
+/* decoded from the packed bytes.                                              */
+/*   acc[b][r] = sum_c t(r, c) * q[b][c]  (int64, asserted to fit int32)       */
+/*   y[b][r]   = (float(acc) * x_scale[b]) * w_scale                           */
+/* Returns 0, -1 for a byte above 242 (not a base-3 byte), -2 on overflow.     */
+/* ------------------------------------------------------------------------- */
+ORACLE_API int oracle_base3_product(const uint8_t *packed, float w_scale, const int8_t *q,
+                                    const float *x_scale, int64_t N, int64_t K, int64_t B,
+                                    int32_t *acc, float *y)
+{
+    int64_t row_bytes = (K + 79) / 80 * 16;
+    for (int64_t r = 0; r < N; r++)
+        for (int64_t i = 0; i < row_bytes; i++)
+            if (packed[r * row_bytes + i] > 242)
+                return -1;
+    for (int64_t b = 0; b < B; b++) {
+        for (int64_t r = 0; r < N; r++) {
+            const uint8_t *row = packed + r * row_bytes;
+            int64_t a = 0;
+            for (int64_t c = 0; c < K; c++) {
+                int t = base3_trit(row, c);
+                if (t == 1)
+                    a += q[b * K + c];
+                else if (t == -1)
+                    a -= q[b * K + c];
+            }
+            if (a > INT32_MAX || a < INT32_MIN)
+                return -2;
+            acc[b * N + r] = (int32_t)a;
+            float tt = (float)a * x_scale[b];
+            y[b * N + r] = tt * w_scale;
+        }
+    }
+    return 0;
+}
+
+/* Every trit of a base-3 packed matrix, [N][K] int8 (reading R15). */
+ORACLE_API void oracle_base3_unpack(const uint8_t *packed, int64_t N, int64_t K, int8_t *out)
+{
+    int64_t row_bytes = (K + 79) / 80 * 16;
+    for (int64_t r = 0; r < N; r++)
+        for (int64_t c = 0; c < K; c++)
+            out[r * K + c] = (int8_t)base3_trit(packed + r * row_bytes, c);
 }

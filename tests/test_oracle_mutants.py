@@ -49,6 +49,10 @@ MUTANTS = [
     ("bf16_ties_away", "(drop == 0x8000u && (keep & 1u))", "(drop == 0x8000u)"),
     ("planar_dequant_swapped_planes", "uint64_t pos = beat[0], neg = beat[1];",
      "uint64_t pos = beat[1], neg = beat[0];"),
+    ("base3_digit_without_offset", "value += (t + 1) * place;", "value += t * place;"),
+    ("base3_high_digit_first", "int j = (int)((col % 80) / 5), i = (int)(col % 5);",
+     "int j = (int)((col % 80) / 5), i = 4 - (int)(col % 5);"),
+    ("base3_group_of_64", "int64_t g = col / 80;", "int64_t g = col / 64;"),
 ]
 
 

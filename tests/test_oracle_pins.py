@@ -453,3 +453,56 @@ def test_trit_planes_dequant_matches_generator_trits():
     bad[0, 0, 0] |= np.uint64(1)
     with pytest.raises(ValueError):
         oracle.trit_planes_dequant(bad, w, K)
+
+
+# ----------------------------------------------------------------------------------------------
+# base-3 packing (reading R15)
+# ----------------------------------------------------------------------------------------------
+def test_base3_golden_bytes():
+    """Bytes worked by hand from the definition ([TR] III.8), placed as bytes 0..5 of the first
+    group of a row whose other columns are zero trits."""
+    gd = read("base3_bytes.txt")
+    K = 128
+    trits = np.zeros((1, K), np.int8)
+    for j in range(6):
+        trits[0, 5 * j: 5 * j + 5] = [int(t) for t in gd[f"trits{j}"].split()]
+    packed = oracle.base3_pack(synth.trits_to_planes(trits), K)
+    assert packed.shape == (1, 32)
+    assert packed[0, :6].tolist() == [int(gd[f"byte{j}"]) for j in range(6)]
+    assert np.all(packed[0, 6:] == 121)       # zero trits, including the padding past K
+
+
+def test_base3_round_trip_and_padding():
+    for K in (64, 320, 2560, 6912):
+        planes, trits = synth.trit_planes(4, K, seed=K)
+        packed = oracle.base3_pack(planes, K)
+        assert packed.shape == (4, (K + 79) // 80 * 16)
+        assert packed.max() <= 242
+        assert np.array_equal(oracle.base3_unpack(packed, K), trits)
+        # the columns past K (to the end of the last 80-column group) hold zero trits
+        tail = (K + 79) // 80 * 80 - K
+        if tail:
+            full = oracle.base3_unpack(packed, (K + 79) // 80 * 80)
+            assert np.all(full[:, K:] == 0)
+
+
+def test_base3_product_equals_planar_and_brute_force():
+    """The base-3 product of the same trits equals the planar oracle's bit for bit, and the
+    accumulators equal a brute-force int64 matmul of the generator's dense trits."""
+    N, K, B = 9, 2560 + 64, 3
+    planes, trits = synth.trit_planes(N, K, seed=91)
+    q = synth.int8_codes(B, K, seed=92, extremes=False)
+    q[0, :] = -128
+    xs = np.array([0.5, 0.013, 3.0], np.float32)
+    acc3, y3 = oracle.base3_product(oracle.base3_pack(planes, K), 0.02, q, xs)
+    accp, yp = oracle.trit_planes_product(planes, 0.02, q, xs)
+    assert np.array_equal(acc3, accp)
+    assert np.array_equal(y3.view(np.uint32), yp.view(np.uint32))
+    assert np.array_equal(acc3.astype(np.int64), q.astype(np.int64) @ trits.astype(np.int64).T)
+
+
+def test_base3_rejects_non_base3_bytes():
+    packed = np.full((1, 16), 121, np.uint8)
+    packed[0, 3] = 243
+    with pytest.raises(ValueError):
+        oracle.base3_product(packed, 1.0, np.zeros((1, 64), np.int8), np.ones(1, np.float32))
