@@ -412,6 +412,7 @@ def rows_measure(lb, out, which: str = "all"):
     if which in ("all", "decode"):
         rows_decode(lb, rows, stream)
         rows_dequant(lb, rows, stream)
+        rows_base3(lb, rows, stream)
     if which in ("all", "prefill"):
         rows_prefill(lb, rows, stream)
     out["rows"] = rows
@@ -557,6 +558,50 @@ def rows_dequant(lb, rows, stream):
                 "GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
                 "us_per_matrix": round(ms * 1e3, 2)}
     del Wq, Wt
+    torch.cuda.empty_cache()
+
+
+def rows_base3(lb, rows, stream):
+    import torch
+    import synth
+    hbm, _ = peaks()
+    # (7) base-3 packing (five trits per byte) against the planar layout on the same trits:
+    #     8 distinct 16384 x 8192 ternary matrices per pass (> L2), per-token int8 activations,
+    #     1 and 8 tokens; GB/s counts each layout's own packed bytes
+    N, K, R = 16384, 8192, 8
+    planes = [synth.device_trit_planes(N, K, 98_000 + r) for r in range(R)]
+    packed = []
+    for t in planes:
+        b3 = torch.empty((N, lb.base3_row_bytes(K)), dtype=torch.uint8, device="cuda")
+        lb.lb_pack_base3(t, N, K, b3, stream=stream)
+        packed.append(b3)
+    torch.cuda.synchronize()
+    pbytes, bbytes = N * K // 4, N * lb.base3_row_bytes(K)
+    out = {}
+    for B in (1, 8):
+        x = torch.from_numpy(synth.activations(B, K, seed=5)).cuda()
+        q = torch.empty((B, K), dtype=torch.int8, device="cuda")
+        xs = torch.empty((B,), dtype=torch.float32, device="cuda")
+        lb.lb_quantize_i8_absmax(x, q, xs, B, K)
+        y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+
+        def b3pass():
+            for w in packed:
+                lb.lb_gemv_base3(w, 0.02, q, xs, y, None, N, K, B, stream=stream)
+
+        def plpass():
+            for w in planes:
+                lb.lb_gemv_trit_planes(w, 0.02, q, xs, y, None, N, K, B, stream=stream)
+        ms3 = time_graph(Graph(b3pass, stream), reps=20) / R
+        msp = time_graph(Graph(plpass, stream), reps=20) / R
+        out[f"b{B}"] = {"base3_us": round(ms3 * 1e3, 2), "planar_us": round(msp * 1e3, 2),
+                        "base3_GB/s": round(bbytes / (ms3 * 1e-3) / 1e9, 1),
+                        "planar_GB/s": round(pbytes / (msp * 1e-3) / 1e9, 1),
+                        "base3_pct_hbm": round(100 * bbytes / (ms3 * 1e-3) / 1e9 / hbm, 1),
+                        "planar_time_over_base3": round(msp / ms3, 3)}
+    out["bytes_per_matrix"] = {"base3": bbytes, "planar": pbytes}
+    rows["base3_vs_planar_16384x8192"] = out
+    del planes, packed
     torch.cuda.empty_cache()
 
 

@@ -23,6 +23,7 @@ __all__ = [
     "lb_gemm_q2_0_g64_grouped", "lb_gemm_q2_0_g64_noalloc", "lb_gemm_trit_workspace_bytes",
     "lb_gemm_trit_planes", "lb_gemm_trit_planes_grouped", "lb_dequantize_q1_0",
     "lb_dequantize_q2_0_g64", "lb_dequantize_trit_planes", "OUT_F32", "OUT_BF16",
+    "lb_pack_base3", "lb_gemv_base3", "base3_row_bytes",
 ]
 
 LB_STATUS = {0: "LB_OK", -1: "LB_ERR_NULL", -2: "LB_ERR_ALIGN", -3: "LB_ERR_SHAPE",
@@ -96,6 +97,8 @@ SIGNATURES = {
     "lb_dequantize_q1_0": (I32, [P, P, I64, I64, I32, P, P]),
     "lb_dequantize_q2_0_g64": (I32, [P, P, I64, I64, I32, P, P]),
     "lb_dequantize_trit_planes": (I32, [P, F32, I64, I64, I32, P, P]),
+    "lb_pack_base3": (I32, [P, I64, I64, P, P]),
+    "lb_gemv_base3": (I32, [P, F32, P, P, P, P, I64, I64, I32, P]),
 }
 
 OUT_F32 = 0
@@ -366,3 +369,20 @@ def lb_dequantize_trit_planes(planes, w_scale: float, N: int, K: int, out_format
     _check("lb_dequantize_trit_planes", load().lb_dequantize_trit_planes(
         _ptr(planes), float(w_scale), int(N), int(K), int(out_format), _ptr(out),
         _stream(stream)))
+
+
+def base3_row_bytes(K: int) -> int:
+    """Bytes per base-3 packed row (LB_BASE3_ROW_BYTES): ceil(K / 80) groups of 16."""
+    return (int(K) + 79) // 80 * 16
+
+
+def lb_pack_base3(planes, N: int, K: int, packed, stream=None):
+    _check("lb_pack_base3", load().lb_pack_base3(_ptr(planes), int(N), int(K), _ptr(packed),
+                                                 _stream(stream)))
+
+
+def lb_gemv_base3(packed, w_scale: float, q, x_scale, y, acc, N: int, K: int, B: int,
+                  stream=None):
+    _check("lb_gemv_base3", load().lb_gemv_base3(
+        _ptr(packed), float(w_scale), _ptr(q), _ptr(x_scale), _ptr(y), _ptr(acc), int(N),
+        int(K), int(B), _stream(stream)))

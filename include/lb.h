@@ -306,6 +306,35 @@ int lb_dequantize_q2_0_g64(const uint8_t *codes, const uint16_t *scales, int64_t
 int lb_dequantize_trit_planes(const uint64_t *planes, float w_scale, int64_t N, int64_t K,
                               int out_format, void *out, void *stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Base-3 packed ternary weights ([TR] III.8: 3^5 = 243 <= 256, five trits per byte, 1.6 bits
+ * per trit; [TA] open questions: base-3 packing against its unpack cost).  The pages fix no
+ * layout; this library's reading: byte j of 16-byte group g of a row holds columns
+ * 80g + 5j + i (i = 0..4) as sum_i (t + 1) * 3^i, the lowest column in the lowest digit; a row
+ * is LB_BASE3_ROW_BYTES(K) = ceil(K/80) * 16 bytes and columns past K hold trit 0.
+ * ------------------------------------------------------------------------------------- */
+#define LB_BASE3_ROW_BYTES(K) ((((K) + 79) / 80) * 16)
+
+/* Load-time packing from the planar layout:
+ *   planes : [N][K/64][2] u64 {pos, neg} (layout of lb_gemv_trit_planes; a column set in both
+ *            planes gives an unspecified byte).
+ *   packed : [N][LB_BASE3_ROW_BYTES(K)] bytes, every byte written (values 0..242).
+ * Like lb_repack_*, it completes before the next kernel of this library starts.
+ * K % 64 == 0, 64 <= K <= 2^24 / 128; 1 <= N <= 2^30. */
+int lb_pack_base3(const uint64_t *planes, int64_t N, int64_t K, uint8_t *packed, void *stream);
+
+/* Decode GEMV on base-3 packed weights, the planar arithmetic ([TA] 1, 4.1, 5):
+ *   acc[b][r] = sum_{c: t = +1} q[b][c] - sum_{c: t = -1} q[b][c]     (int32, exact)
+ *   y[b][r]   = (float(acc) * x_scale[b]) * w_scale                    (two roundings)
+ * bit-identical to lb_gemv_trit_planes on the same trits.  A byte above 242 (never written by
+ * lb_pack_base3) gives an unspecified, in-bounds result.
+ *   packed : [N][LB_BASE3_ROW_BYTES(K)] (lb_pack_base3).   q : [B][K] int8.
+ *   x_scale : [B] fp32.   y : [B][N] fp32.   acc_opt : NULL or [B][N] int32.
+ * K % 64 == 0, 64 <= K <= 2^24 / 128; 1 <= N <= 2^30; B in [1, 8]; shared memory bounds the
+ * activation: 32 KB + B * ceil(K/80) * 80 bytes must stay within 200 KB (LB_ERR_SHAPE). */
+int lb_gemv_base3(const uint8_t *packed, float w_scale, const int8_t *q, const float *x_scale,
+                  float *y, int32_t *acc_opt, int64_t N, int64_t K, int B, void *stream);
+
 /* ---- Q2_0_g64 prefill GEMM without caller scratch.
  * No counterpart in the source pages: a convenience of this library for callers that cannot
  * allocate device memory.  Same arithmetic, accuracy, layouts and errors as lb_gemm_q2_0_g64,

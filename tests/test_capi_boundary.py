@@ -263,3 +263,21 @@ def test_dequant_trit_refusals(lib):
     assert f(A, 1.0, 4, 64, 0, MIS, None) == -2
     assert f(A, 1.0, 4, 96, 0, A, None) == -3
     assert f(A, 1.0, 4, 64, 3, A, None) == -3
+
+
+# ---- base-3 packing: host checks ----
+def test_base3_refusals(lib):
+    assert lib.lb_pack_base3(None, 4, 64, A, None) == -1
+    assert lib.lb_pack_base3(A, 4, 64, MIS, None) == -2
+    assert lib.lb_pack_base3(A, 4, 96, A, None) == -3
+    assert lib.lb_pack_base3(A, 0, 64, A, None) == -3
+    g = lib.lb_gemv_base3
+    assert g(None, 1.0, A, A, A, None, 4, 64, 1, None) == -1
+    assert g(A, 1.0, A, A, MIS, None, 4, 64, 1, None) == -2
+    assert g(A, 1.0, A, A, A, MIS, 4, 64, 1, None) == -2
+    assert g(A, 1.0, A, A, A, None, 4, 80, 1, None) == -3
+    assert g(A, 1.0, A, A, A, None, 4, 64, 0, None) == -4
+    assert g(A, 1.0, A, A, A, None, 4, 64, 9, None) == -4
+    # 8 tokens of 32768 columns: 8 * 410 * 80 bytes of activation image exceed the limit
+    assert g(A, 1.0, A, A, A, None, 4, 32768, 8, None) == -3
+    assert lb.base3_row_bytes(2560) == 512 and lb.base3_row_bytes(6912) == 1392
