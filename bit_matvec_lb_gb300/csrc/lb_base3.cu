@@ -152,11 +152,16 @@ __global__ void __launch_bounds__(kB3Threads) gemv_base3_kernel(const __grid_con
 
     for (int64_t r0 = ((int64_t)blockIdx.x * kB3Warps + warp) * kB3RowsPerWarp; r0 < p.N;
          r0 += nwarps * kB3RowsPerWarp) {
-        int acc[kB3RowsPerWarp][B];
+        // NA independent partial sums per row and token (at 1-2 tokens the dp4a chains of one
+        // row would otherwise be a single serial dependence)
+        constexpr int NA = B <= 2 ? 4 : 1;
+        int acc[kB3RowsPerWarp][B][NA];
 #pragma unroll
         for (int rr = 0; rr < kB3RowsPerWarp; rr++)
 #pragma unroll
-            for (int b = 0; b < B; b++) acc[rr][b] = 0;
+            for (int b = 0; b < B; b++)
+#pragma unroll
+                for (int c = 0; c < NA; c++) acc[rr][b][c] = 0;
         for (int g0 = 0; g0 < G; g0 += 32 * kB3GroupsPerLane) {
             uint4 wv[kB3RowsPerWarp][kB3GroupsPerLane];
             // every load of the batch first (rows past N and groups past G read nothing)
@@ -191,12 +196,12 @@ __global__ void __launch_bounds__(kB3Threads) gemv_base3_kernel(const __grid_con
                         for (int b = 0; b < B; b++) {
                             const uint4 av = a[(int64_t)b * G * 5 + u];
                             const uint32_t a5 = b3_word(a[(int64_t)b * G * 5 + 4], u);
-                            int s = acc[rr][b];
+                            int s = acc[rr][b][u % NA];
                             s = dp4a_ss(e[0].x, av.x, s);
                             s = dp4a_ss(e[1].x, av.y, s);
                             s = dp4a_ss(e[2].x, av.z, s);
                             s = dp4a_ss(e[3].x, av.w, s);
-                            acc[rr][b] = dp4a_ss(w4, a5, s);
+                            acc[rr][b][u % NA] = dp4a_ss(w4, a5, s);
                         }
                     }
                 }
@@ -206,18 +211,20 @@ __global__ void __launch_bounds__(kB3Threads) gemv_base3_kernel(const __grid_con
         for (int rr = 0; rr < kB3RowsPerWarp; rr++) {
 #pragma unroll
             for (int b = 0; b < B; b++) {
-                int s = acc[rr][b];
+                int s = acc[rr][b][0];
+#pragma unroll
+                for (int c = 1; c < NA; c++) s += acc[rr][b][c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                acc[rr][b] = s;
+                acc[rr][b][0] = s;
             }
             const int64_t r = r0 + rr;
             if (lane == 0 && r < p.N) {
 #pragma unroll
                 for (int b = 0; b < B; b++) {
-                    const float f = (float)acc[rr][b];
+                    const float f = (float)acc[rr][b][0];
                     p.y[(int64_t)b * p.N + r] = __fmul_rn(__fmul_rn(f, xs[b]), p.w_scale);
-                    if (p.acc) p.acc[(int64_t)b * p.N + r] = acc[rr][b];
+                    if (p.acc) p.acc[(int64_t)b * p.N + r] = acc[rr][b][0];
                 }
             }
         }

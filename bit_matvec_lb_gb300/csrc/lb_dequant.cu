@@ -6,10 +6,10 @@
 // (Q1_0: w = +1 for a set bit, -1 otherwise), III.5 (Q2_0_g64: w = code - 1).  Planar weights
 // (tritium.technology "Architecture", section 2) dequantize to w * w_scale, w in {+1, -1, 0}.
 //
-// HBM-bound streaming kernel: a group of 8 threads takes one 32-column group of one row (the
-// packed word is read once per group and broadcast), each thread writes 4 consecutive outputs,
-// so every warp stores 512 contiguous bytes (fp32) or 256 (bf16); every thread keeps several
-// groups' loads in flight.  Blocks take whole rows, so indices need no division.
+// HBM-bound streaming kernel: a group of 8 threads (4 for bf16) takes one 32-column group of one
+// row (the packed word is read once per group and broadcast), each thread writes one 16-byte
+// vector of consecutive outputs, so every warp stores 512 contiguous bytes; every thread keeps
+// several groups' loads in flight.  Blocks take whole rows, so indices need no division.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -68,8 +68,10 @@ __device__ __forceinline__ void dq_values(const DqIn<F> &in, int part, float (&v
 }
 
 // A block takes whole rows (rows blockIdx.x, blockIdx.x + gridDim.x, ...).  Within a row, slot t
-// = 8 g + part writes columns 4 part .. 4 part + 3 of group g, so no index needs a division;
-// each thread takes kU slots per iteration, their loads issued before any conversion.
+// = TPG g + part writes columns OUT part .. OUT part + OUT - 1 of group g (TPG threads per
+// 32-column group, OUT = 32 / TPG outputs each: 4 fp32 or 8 bf16, one 16-byte store), so no
+// index needs a division; each thread takes kU slots per iteration, their loads issued before
+// any conversion.
 constexpr int kU = 4;
 
 template <int F, bool BF16>
@@ -77,30 +79,41 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
                                                       const uint16_t *__restrict__ scales,
                                                       float w_scale, void *__restrict__ out,
                                                       int64_t N, int64_t K, int S) {
+    constexpr int TPG = BF16 ? 4 : 8;
+    constexpr int LOG_TPG = BF16 ? 2 : 3;
     pdl_launch_dependents();
     pdl_wait();
-    const int slots = (int)(K / 32) * 8;  // 8 threads per 32-column group
+    const int slots = (int)(K / 32) * TPG;
     for (int64_t n = blockIdx.x; n < N; n += gridDim.x) {
         for (int t0 = threadIdx.x; t0 < slots; t0 += kU * blockDim.x) {
             DqIn<F> in[kU];
 #pragma unroll
             for (int u = 0; u < kU; u++) {
                 const int t = t0 + u * (int)blockDim.x;
-                if (t < slots) in[u] = dq_load<F>(w, scales, w_scale, n, t >> 3, K, S);
+                if (t < slots) in[u] = dq_load<F>(w, scales, w_scale, n, t >> LOG_TPG, K, S);
             }
 #pragma unroll
             for (int u = 0; u < kU; u++) {
                 const int t = t0 + u * (int)blockDim.x;
                 if (t >= slots) break;
-                float v[4];
-                dq_values<F>(in[u], t & 7, v);
-                const int64_t o = n * K + (int64_t)(t >> 3) * 32 + 4 * (t & 7);
+                const int part = t & (TPG - 1);
+                const int64_t o = n * K + (int64_t)(t >> LOG_TPG) * 32 + (32 / TPG) * part;
                 if (BF16) {
-                    __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
-                    __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
-                    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + o) = make_uint2(
-                        *reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                    float v0[4], v1[4];
+                    dq_values<F>(in[u], 2 * part, v0);
+                    dq_values<F>(in[u], 2 * part + 1, v1);
+                    __nv_bfloat162 h[4] = {__floats2bfloat162_rn(v0[0], v0[1]),
+                                           __floats2bfloat162_rn(v0[2], v0[3]),
+                                           __floats2bfloat162_rn(v1[0], v1[1]),
+                                           __floats2bfloat162_rn(v1[2], v1[3])};
+                    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o) =
+                        make_uint4(*reinterpret_cast<uint32_t *>(&h[0]),
+                                   *reinterpret_cast<uint32_t *>(&h[1]),
+                                   *reinterpret_cast<uint32_t *>(&h[2]),
+                                   *reinterpret_cast<uint32_t *>(&h[3]));
                 } else {
+                    float v[4];
+                    dq_values<F>(in[u], part, v);
                     *reinterpret_cast<float4 *>(static_cast<float *>(out) + o) =
                         make_float4(v[0], v[1], v[2], v[3]);
                 }
