@@ -533,22 +533,23 @@ def rows_dequant(lb, rows, stream):
     import synth
     hbm, _ = peaks()
     # (6) load-time dequantization, HBM-bound: 16 distinct 4096 x 4096 matrices per pass
-    #     (> L2), Q2_0_g64 and planar, to fp32 and bf16; bytes = packed weights + scales read
-    #     + outputs written
+    #     (> L2), Q2_0_g64 and planar, to fp32 and bf16, each into its own output buffer (so
+    #     the written bytes leave the L2 too); bytes = packed weights + scales read + outputs
+    #     written
     N, K, R = ROWS_N, ROWS_K, 16
     Wq = [make_q2_weights(N, K, 96_000 + r) for r in range(R)]
     Wt = [synth.device_trit_planes(N, K, 97_000 + r) for r in range(R)]
     for fmt, esz in ((lb.OUT_F32, 4), (lb.OUT_BF16, 2)):
-        out = torch.empty((N, K), dtype=torch.float32 if esz == 4 else torch.int16,
-                          device="cuda")
+        outs = [torch.empty((N, K), dtype=torch.float32 if esz == 4 else torch.int16,
+                            device="cuda") for _ in range(R)]
         name = "f32" if esz == 4 else "bf16"
 
         def q2pass():
-            for c, s in Wq:
+            for (c, s), out in zip(Wq, outs):
                 lb.lb_dequantize_q2_0_g64(c, s, N, K, fmt, out, stream=stream)
 
         def tpass():
-            for t in Wt:
+            for t, out in zip(Wt, outs):
                 lb.lb_dequantize_trit_planes(t, 0.02, N, K, fmt, out, stream=stream)
         for label, fn, wbytes in (("q2_0_g64", q2pass, q2_bytes(N, K) + N * scale_stride(K, 64) * 2 - N * (K // 64) * 2),
                                   ("trit_planes", tpass, N * K // 64 * 16)):
@@ -557,6 +558,7 @@ def rows_dequant(lb, rows, stream):
             rows[f"dequant_{label}_4096x4096_{name}"] = {
                 "GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
                 "us_per_matrix": round(ms * 1e3, 2)}
+        del outs
     del Wq, Wt
     torch.cuda.empty_cache()
 
