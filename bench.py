@@ -191,10 +191,10 @@ def profiled_traffic(path_name: str):
 # ---------------------------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample, all host cores, rows split across threads)
 # ---------------------------------------------------------------------------------------------
-def oracle_gbs(blocks_np: np.ndarray, q, dx, budget_s: float, qk: int = 64):
+def oracle_gbs(blocks_np: np.ndarray, q, dx, budget_s: float, qk: int = 64, threads=None):
     import oracle
     fn = oracle.q2_0_g64_product if qk == 64 else oracle.q1_0_product
-    cores = len(os.sched_getaffinity(0))
+    cores = threads or len(os.sched_getaffinity(0))
     N = blocks_np.shape[0]
     chunks = [blocks_np[i:i + max(1, N // cores)] for i in range(0, N, max(1, N // cores))]
     fn(blocks_np[:8], q, dx, want_isum=False)  # build / warm
@@ -248,6 +248,29 @@ def time_graph(graph: Graph, reps: int, warm: int = 3) -> float:
         e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / reps
+
+
+def read_probe(stream, nbytes: int = 1 << 30, reps: int = 10):
+    """Read-only HBM bandwidth in this process: torch's sum over a 1 GiB buffer (a library
+    kernel, reads only), beside the measured copy peak that the roofline divides by."""
+    import torch
+    try:
+        buf = torch.ones(nbytes // 4, dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                buf.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                buf.sum()
+            e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        del buf
+        return {"GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                "what": "torch.sum over 1 GiB fp32 (read only), CUDA events, same process"}
+    except Exception as e:  # the probe is context; it never fails the bench line
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
 
 
 def make_q2_weights(N, K, seed, device="cuda"):
@@ -348,6 +371,7 @@ def headline(lb, args, dist, out):
     achieved = alg_bytes / (ms_gemv * 1e-3) / 1e9
     ms_single = time_graph(Graph(gemvs_single, stream), reps=max(20, args.steps // 20)) / N_ROT
     traffic = profiled_traffic("stream_gemv_q2_0_g64_4096x4096_b1.md")
+    probe = read_probe(stream)
 
     # ---- e2e: pinned host activation in, outputs out, every step ----
     x_host = torch.from_numpy(x_np).pin_memory()
@@ -384,6 +408,8 @@ def headline(lb, args, dist, out):
         "clocks": clocks,
         "gpu_launches": int(args.steps * 2),
         "pct_hbm": round(100 * value / dist.world / hbm, 2),
+        "read_probe": dict(probe, **({"gemv_launch_frac": round(achieved / probe["GB/s"], 4)}
+                                     if "GB/s" in probe else {})),
         "single_launch": {"GB/s": round(q2_bytes(N, K) / (ms_single * 1e-3) / 1e9, 1),
                           "us_per_gemv": round(ms_single * 1e3, 3),
                           "note": "the same 64 GEMVs as 64 single-matrix launches (PDL-chained)"},
@@ -392,11 +418,17 @@ def headline(lb, args, dist, out):
     if dist.rank == 0:
         q_ref2 = q_ref
         gbs, cores, reps, dt = oracle_gbs(blocks0[:512], q_ref2, d_ref, budget_s=args.cpu_budget)
+        gbs1, _, reps1, dt1 = oracle_gbs(blocks0[:64], q_ref2, d_ref,
+                                         budget_s=max(1.0, args.cpu_budget / 4), threads=1)
         out["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
                                "kind": "oracle",
                                "sample": f"rows 0..511 of one 4096x4096 Q2_0_g64 matrix, batch 1, "
                                          f"rows split over {cores} threads, {reps} passes in "
-                                         f"{dt:.1f} s"}
+                                         f"{dt:.1f} s",
+                               "single_thread": {"value": round(gbs1, 4), "unit": "GB/s",
+                                                 "cores": 1,
+                                                 "sample": f"rows 0..63, {reps1} passes in "
+                                                           f"{dt1:.1f} s"}}
     del W, g_step, g_gemv
     torch.cuda.empty_cache()
 
