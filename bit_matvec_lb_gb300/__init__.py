@@ -23,7 +23,7 @@ __all__ = [
     "lb_gemm_q2_0_g64_grouped", "lb_gemm_q2_0_g64_noalloc", "lb_gemm_trit_workspace_bytes",
     "lb_gemm_trit_planes", "lb_gemm_trit_planes_grouped", "lb_dequantize_q1_0",
     "lb_dequantize_q2_0_g64", "lb_dequantize_trit_planes", "OUT_F32", "OUT_BF16",
-    "lb_pack_base3", "lb_gemv_base3", "base3_row_bytes",
+    "lb_pack_base3", "lb_gemv_base3", "base3_row_bytes", "lb_test_inject_wait_timeout",
 ]
 
 LB_STATUS = {0: "LB_OK", -1: "LB_ERR_NULL", -2: "LB_ERR_ALIGN", -3: "LB_ERR_SHAPE",
@@ -78,6 +78,7 @@ SIGNATURES = {
     "lb_gemv_trit_planes": (I32, [P, F32, P, P, P, P, I64, I64, I32, P]),
     "lb_gemv_bf16": (I32, [P, P, P, I64, I64, I32, P]),
     "lb_device_status": (I32, [P]),
+    "lb_test_inject_wait_timeout": (I32, [I32]),
     "lb_gemv_q1_0_grouped": (I32, [ctypes.POINTER(lb_q_matrix), I32, P, P, I64, I32, P]),
     "lb_gemv_q2_0_g64_grouped": (I32, [ctypes.POINTER(lb_q_matrix), I32, P, P, I64, I32, P]),
     "lb_gemv_trit_planes_grouped": (I32, [ctypes.POINTER(lb_trit_matrix), I32, P, P, I64, I32,
@@ -227,6 +228,12 @@ def lb_gemv_bf16(w, x, y, N: int, K: int, B: int, stream=None):
 def lb_device_status(stream=None) -> int:
     """Synchronize the stream and return (and clear) the device error status (0 = OK)."""
     return load().lb_device_status(_stream(stream))
+
+
+def lb_test_inject_wait_timeout(wait_us: int):
+    """Test hook: the next streaming GEMV call starves its first CTA, whose bounded wait then
+    gives up after wait_us microseconds (reported by lb_device_status as LB_ERR_DEVICE)."""
+    _check("lb_test_inject_wait_timeout", load().lb_test_inject_wait_timeout(int(wait_us)))
 
 
 def _q_mats(mats):

@@ -9,6 +9,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -51,6 +52,10 @@ int current_device_info(DeviceInfo *out) {
     }
     return out->ok == 1 ? LB_OK : LB_ERR_ARCH;
 }
+
+static std::atomic<int> g_injected_wait_us{0};
+
+int take_injected_wait_fault() { return g_injected_wait_us.exchange(0); }
 
 // One error word per device (file-scope device variable; the host passes its address).
 __device__ int g_device_error;
@@ -176,6 +181,12 @@ LB_EXPORT const char *lb_status_string(int status) {
 }
 
 LB_EXPORT int lb_version(void) { return 100; }
+
+LB_EXPORT int lb_test_inject_wait_timeout(int wait_us) {
+    if (wait_us < 1 || wait_us > 1000000) return LB_ERR_SHAPE;
+    lb::g_injected_wait_us.store(wait_us);
+    return LB_OK;
+}
 
 LB_EXPORT int lb_device_status(void *stream) {
     using namespace lb;

@@ -43,6 +43,11 @@ inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s
 int encode_rows_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows,
                     uint32_t box_bytes, uint32_t box_rows, int swizzle_bytes = 0);
 
+// Test hook: the wait limit in microseconds set by lb_test_inject_wait_timeout (then cleared),
+// or 0.  A streaming GEMV launch that takes a non-zero value makes CTA 0 copy no weights, so
+// that CTA's consumers give up after that many microseconds and report through the error word.
+int take_injected_wait_fault();
+
 // Remember a failed CUDA call's error for lb_last_cuda_error() (calling thread) and clear it
 // from the runtime's last-error slot.
 void record_cuda_error(cudaError_t e);

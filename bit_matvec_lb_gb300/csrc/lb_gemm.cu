@@ -465,6 +465,13 @@ static int gemm_q_group(int F, const lb_gemm_matrix *mats, int G, const int8_t *
     }
     DeviceInfo di;
     if (int st = current_device_info(&di)) return st;
+    p.err = device_error_word();
+    if (!p.err) return LB_ERR_LAUNCH;
+    auto kern = F == kG1 ? gemm_q_kernel<kG1> : gemm_q_kernel<kG2>;
+    int bps = 0;
+    if (int e2 = prepare_kernel(reinterpret_cast<const void *>(kern), kGemmThreads, kGemmSmem,
+                                &bps))
+        return e2;
     cudaStream_t st = as_stream(stream);
     // prologue: activation tiles
     const int64_t work = mtiles * kTileM * (K / 32);
@@ -479,18 +486,12 @@ static int gemm_q_group(int F, const lb_gemm_matrix *mats, int G, const int8_t *
     if (e) return e;
     p.ws = (const uint8_t *)workspace;
     p.d = d;
-    p.err = device_error_word();
     p.G = G;
     p.M = (int)M;
     p.K = (int)K;
     p.S = (int)((K / qk + 7) / 8 * 8);
     p.nK32 = (int)(K / 32);
     p.mtiles = (int)mtiles;
-    auto kern = F == kG1 ? gemm_q_kernel<kG1> : gemm_q_kernel<kG2>;
-    int bps = 0;
-    if (int e2 = prepare_kernel(reinterpret_cast<const void *>(kern), kGemmThreads, kGemmSmem,
-                                &bps))
-        return e2;
     return launch_pdl(kern, dim3((unsigned)tiles), dim3(kGemmThreads), kGemmSmem, st, p);
 }
 
@@ -914,6 +915,12 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
     ks = (nst + sps - 1) / sps;
     DeviceInfo di;
     if (int st = current_device_info(&di)) return st;
+    p.err = device_error_word();
+    if (!p.err) return LB_ERR_LAUNCH;
+    int bps = 0;
+    if (int e = prepare_kernel(reinterpret_cast<const void *>(gemm_trit_kernel), kTritThreads,
+                               kTritSmem, &bps))
+        return e;
     cudaStream_t st = as_stream(stream);
     const int64_t work = mtiles * kTileM * (K / 32);
     int64_t pgrid = (work + 255) / 256;
@@ -923,17 +930,12 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
         return e;
     p.ws = static_cast<const uint8_t *>(workspace);
     p.x_scale = x_scale;
-    p.err = device_error_word();
     p.G = G;
     p.M = (int)M;
     p.nst = nst;
     p.mtiles = (int)mtiles;
     p.ks = ks;
     p.sps = sps;
-    int bps = 0;
-    if (int e = prepare_kernel(reinterpret_cast<const void *>(gemm_trit_kernel), kTritThreads,
-                               kTritSmem, &bps))
-        return e;
     // The ks splits of a tile are consecutive blocks and form one cluster.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles * ks));

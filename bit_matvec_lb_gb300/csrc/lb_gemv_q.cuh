@@ -40,6 +40,7 @@ inline int gemv_q_grouped(const lb_q_matrix *mats, int G, const int8_t *q, const
     p.q = q;
     p.d = d;
     p.err = device_error_word();
+    if (!p.err) return LB_ERR_LAUNCH;
     p.K = K;
     p.nchunk = (int32_t)(K / qk);
     p.S = (int32_t)scale_stride(K, qk);

@@ -34,6 +34,7 @@ LB_EXPORT int lb_gemv_trit_planes_grouped(const lb_trit_matrix *mats, int G, con
     p.q = q;
     p.x_scale = x_scale;
     p.err = device_error_word();
+    if (!p.err) return LB_ERR_LAUNCH;
     p.K = K;
     p.nchunk = (int32_t)(K / 64);
     p.S = 0;

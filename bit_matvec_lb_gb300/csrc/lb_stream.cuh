@@ -85,8 +85,11 @@ struct StreamParams {
     const float *x_scale;     // [B] (planar)
     int *err;                 // device error word
     int64_t K;
-    int32_t G, nunits, nct, KC, nchunk, S, stages, stage_bytes, act_bytes, pad;
+    int32_t G, nunits, nct, KC, nchunk, S, stages, stage_bytes, act_bytes;
+    int32_t fault;            // test hook: 0, or the consumers' wait limit in us (CTA 0 starves)
 };
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // every wait gives up after about 2 s
 
 // ------------------------------------------------------------------------------------------
 // Activation staging (consumer threads only).  One thread per 32-value group.
@@ -216,8 +219,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     }
     __syncthreads();
     pdl_launch_dependents();
+    // Test hook (lb_test_inject_wait_timeout): CTA 0's producer copies nothing, so its
+    // consumers' first wait runs out after p.fault microseconds; they report and stop.
+    const uint64_t wait_ns = p.fault ? (uint64_t)p.fault * 1000u : kWaitLimitNs;
 
     if (warp == kConsumerWarps) {
+        if (p.fault && blockIdx.x == 0) return;
         // ---------------- producer warp: stream row tiles into the stage ring ----------------
         int stage = 0;
         uint32_t phase = 0;
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         for (int ct = 0; ct < p.nct; ct++) {
             const int c0 = ct * KC;
             const int kc = min(KC, p.nchunk - c0);
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, wait_ns))) {
                 if (lane == 0) report(p.err);
                 return;
             }
@@ -528,8 +535,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     }
     __syncthreads();
     pdl_launch_dependents();
+    // Test hook, as in stream_gemv_kernel.
+    const uint64_t wait_ns = p.fault ? (uint64_t)p.fault * 1000u : kWaitLimitNs;
 
     if (warp == kConsumerWarps) {
+        if (p.fault && blockIdx.x == 0) return;
         // ---------------- producer warp: lane r copies row r of every stage ----------------
         int stage = 0;
         uint32_t phase = 0;
@@ -599,7 +609,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         for (int ct = 0; ct < p.nct; ct++) {
             const int c0 = ct * KC;
             const int kc = min(KC, p.nchunk - c0);
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, wait_ns))) {
                 if (lane == 0) report(p.err);
                 return;
             }
@@ -784,6 +794,7 @@ constexpr int64_t kTcMinUnits = 64;
 
 template <int F>
 inline int dispatch_stream(StreamParams &p, int B, bool aux, int sms, cudaStream_t st) {
+    p.fault = 0;
     // Three or more tokens: the tensor-core variant (lb_tcgemv.cuh) when K is a multiple of
     // its 256-column step, its activation operand (16 K bytes) fits in shared memory and the
     // call has at least kTcMinUnits row units; the block-sum hook stays on the streaming
@@ -800,6 +811,7 @@ inline int dispatch_stream(StreamParams &p, int B, bool aux, int sms, cudaStream
             case 8: return launch_tc_gemv<F, 8>(p, sms, st);
         }
     }
+    p.fault = take_injected_wait_fault();  // only the streaming kernels honor the test hook
     switch (B) {
         case 1: return launch_stream<F, 1>(p, aux, sms, st);
         case 2: return launch_stream<F, 2>(p, aux, sms, st);

@@ -68,10 +68,20 @@ const char *lb_cuda_error_name(int code);
 /* Library version as 10000*major + 100*minor + patch. */
 int lb_version(void);
 
-/* Synchronizes `stream`, then reads and clears the current device's error word.  Returns LB_OK,
+/* Synchronizes `stream`, then reads and clears the current device's error word (a device
+ * variable of the library whose address is looked up once per device and kept: do not use the
+ * library across cudaDeviceReset).  Returns LB_OK,
  * or LB_ERR_DEVICE if a kernel of this library gave up on a bounded wait since the last call
  * (its outputs are then incomplete).  Kernels never hang: every wait gives up after about 2 s. */
 int lb_device_status(void *stream);
+
+/* Test hook for failure detection: the next Q1_0 / Q2_0_g64 / planar GEMV call (plain or
+ * grouped) that runs on the streaming or lane-per-row kernel (1-2 tokens, or 3-8 tokens outside
+ * the tensor-core kernel's shapes) makes its first CTA copy no weights, so that CTA's bounded
+ * wait gives up after `wait_us` microseconds instead of about 2 s: the call then leaves part of
+ * y unwritten and lb_device_status() reports LB_ERR_DEVICE.  Nothing faults, traps or hangs.
+ * One-shot, process-wide.  1 <= wait_us <= 10^6, else LB_ERR_SHAPE.  Not for production use. */
+int lb_test_inject_wait_timeout(int wait_us);
 
 /* ---------------------------------------------------------------------------------------
  * Activation quantizers
@@ -345,8 +355,12 @@ int lb_gemv_base3(const uint8_t *packed, float w_scale, const int8_t *q, const f
  *   device work.  Nothing in the scratch needs to start at zero.
  *   There is one scratch per device: calls that may run at the same time on one device (another
  *   stream, another host thread) race on it and give wrong results; serialize them.
- *   The first call on each device looks the scratch up (cudaGetSymbolAddress); make that first
- *   call before capturing a stream into a CUDA graph. */
+ *   The first call on each device looks the scratch up (cudaGetSymbolAddress).  Under lazy
+ *   module loading that lookup may load the library's device code, and the driver then
+ *   reserves the 8 MiB array: a one-time allocation by the driver, not by this call.  Make one
+ *   warm-up call per device before an allocation-free region or a stream capture.
+ *   The looked-up address is kept for the life of the process: do not use the library across
+ *   cudaDeviceReset (the same holds for every entry point's device error word). */
 #define LB_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 int lb_gemm_q2_0_g64_noalloc(const uint8_t *codes, const uint16_t *scales, const int8_t *q,

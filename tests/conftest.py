@@ -16,3 +16,11 @@ def pytest_configure(config):
 def pytest_collection_modifyitems(config, items):
     # GPU tests fail loudly (not skip) when run without a GPU: -m gpu is only run on a GPU machine.
     pass
+
+
+@pytest.fixture(autouse=True)
+def _output_guard_bands():
+    """After every test: no kernel wrote into the sentinel bands around its output buffers."""
+    yield
+    if "gpu_util" in sys.modules:
+        sys.modules["gpu_util"].check_guards()

@@ -281,3 +281,10 @@ def test_base3_refusals(lib):
     # 8 tokens of 32768 columns: 8 * 410 * 80 bytes of activation image exceed the limit
     assert g(A, 1.0, A, A, A, None, 4, 32768, 8, None) == -3
     assert lb.base3_row_bytes(2560) == 512 and lb.base3_row_bytes(6912) == 1392
+
+
+def test_injected_wait_limit_is_range_checked(lib):
+    # the failure-detection hook refuses limits outside [1 us, 1 s] on the host
+    assert lib.lb_test_inject_wait_timeout(0) == -3
+    assert lib.lb_test_inject_wait_timeout(2_000_000) == -3
+    assert lib.lb_test_inject_wait_timeout(-5) == -3

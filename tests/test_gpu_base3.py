@@ -10,14 +10,14 @@ import torch
 import bit_matvec_lb_gb300 as lb
 import oracle
 import synth
-from gpu_util import dev, host
+from gpu_util import dev, guarded, host
 
 pytestmark = pytest.mark.gpu
 
 
 def pack_gpu(planes, K):
     N = planes.shape[0]
-    packed = torch.full((N, lb.base3_row_bytes(K)), 255, dtype=torch.uint8, device="cuda")
+    packed = guarded((N, lb.base3_row_bytes(K)), torch.uint8, 255)
     lb.lb_pack_base3(dev(planes), N, K, packed)
     torch.cuda.synchronize()
     return packed
@@ -25,8 +25,8 @@ def pack_gpu(planes, K):
 
 def gemv_b3(packed, w_scale, q, xs, N, K):
     B = q.shape[0]
-    y = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
-    acc = torch.full((B, N), -7, dtype=torch.int32, device="cuda")
+    y = guarded((B, N), torch.float32, float("nan"))
+    acc = guarded((B, N), torch.int32, -7)
     lb.lb_gemv_base3(packed, w_scale, dev(q), dev(np.asarray(xs, np.float32)), y, acc, N, K, B)
     torch.cuda.synchronize()
     return host(acc), host(y)
@@ -61,8 +61,8 @@ def test_gemv_base3_extremes_and_planar_equality():
     acc, y = gemv_b3(pack_gpu(planes, K), 1.0, q, xs, N, K)
     acc_ref, y_ref = oracle.base3_product(oracle.base3_pack(planes, K), 1.0, q, xs)
     assert np.array_equal(acc, acc_ref) and np.array_equal(y.view(np.uint32), y_ref.view(np.uint32))
-    yp = torch.empty((B, N), dtype=torch.float32, device="cuda")
-    ap = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    yp = guarded((B, N), torch.float32)
+    ap = guarded((B, N), torch.int32)
     lb.lb_gemv_trit_planes(dev(planes), 1.0, dev(q), dev(xs), yp, ap, N, K, B)
     torch.cuda.synchronize()
     assert np.array_equal(acc, host(ap)) and np.array_equal(y.view(np.uint32),

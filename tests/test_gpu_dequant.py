@@ -10,14 +10,14 @@ import torch
 import bit_matvec_lb_gb300 as lb
 import oracle
 import synth
-from gpu_util import dev, host, repack_on_gpu
+from gpu_util import dev, guarded, host, repack_on_gpu
 
 pytestmark = pytest.mark.gpu
 
 
 def _run(fn, args, N, K, fmt):
     dtype = torch.float32 if fmt == lb.OUT_F32 else torch.int16
-    out = torch.full((N, K), -1, dtype=dtype, device="cuda")
+    out = guarded((N, K), dtype, -1)
     fn(*args, N, K, fmt, out)
     torch.cuda.synchronize()
     return host(out, np.uint32 if fmt == lb.OUT_F32 else np.uint16)

@@ -16,7 +16,7 @@ import torch
 import bit_matvec_lb_gb300 as lb
 import oracle
 import synth
-from gpu_util import dev, gemm_q, repack_on_gpu, within
+from gpu_util import dev, gemm_q, guarded, repack_on_gpu, within
 
 pytestmark = pytest.mark.gpu
 
@@ -131,7 +131,7 @@ def test_gemm_workspace_reused(qk):
     N, K = 200, 2048
     blocks = _blocks(qk, N, K, seed=71)
     rep = repack_on_gpu(blocks, K, qk)
-    ws = torch.empty(lb.lb_gemm_workspace_bytes(300, K), dtype=torch.uint8, device="cuda")
+    ws = guarded(lb.lb_gemm_workspace_bytes(300, K), torch.uint8)
     for M, seed in ((300, 72), (77, 73)):
         q, dx = oracle.quantize_q8_0(synth.activations(M, K, seed=seed))
         y = gemm_q(qk, blocks, q, dx, workspace=ws, repacked=rep)
@@ -162,12 +162,12 @@ def test_gemm_grouped(qk):
     call on the same weights."""
     M, K, Ns = 130, 1152 if qk == 128 else 1216, (130, 1, 257)
     q, dx = oracle.quantize_q8_0(synth.activations(M, K, seed=940))
-    ws = torch.empty(lb.lb_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    ws = guarded(lb.lb_gemm_workspace_bytes(M, K), torch.uint8)
     mats, outs = [], []
     for i, n in enumerate(Ns):
         blocks = _blocks(qk, n, K, seed=950 + i)
         bits, scales = repack_on_gpu(blocks, K, qk)
-        y = torch.full((M, n), float("nan"), dtype=torch.float32, device="cuda")
+        y = guarded((M, n), torch.float32, float("nan"))
         mats.append((bits, scales, y, n))
         outs.append((blocks, bits, scales, y))
     fn = lb.lb_gemm_q1_0_grouped if qk == 128 else lb.lb_gemm_q2_0_g64_grouped

@@ -17,7 +17,7 @@ import torch
 import bit_matvec_lb_gb300 as lb
 import oracle
 import synth
-from gpu_util import dev, host
+from gpu_util import dev, guarded, host
 
 pytestmark = pytest.mark.gpu
 
@@ -31,10 +31,9 @@ def gemm_trit(planes, w_scale, q, xs, workspace=None, planes_dev=None):
     N = planes.shape[0]
     M, K = q.shape
     if workspace is None:
-        workspace = torch.empty(lb.lb_gemm_trit_workspace_bytes(M, K), dtype=torch.uint8,
-                                device="cuda")
-    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-    acc = torch.full((M, N), -7, dtype=torch.int32, device="cuda")
+        workspace = guarded(lb.lb_gemm_trit_workspace_bytes(M, K), torch.uint8)
+    y = guarded((M, N), torch.float32, float("nan"))
+    acc = guarded((M, N), torch.int32, -7)
     lb.lb_gemm_trit_planes(dev(planes) if planes_dev is None else planes_dev, w_scale, dev(q),
                            dev(np.asarray(xs, np.float32)), y, acc, M, N, K, workspace)
     torch.cuda.synchronize()
@@ -98,8 +97,8 @@ def test_gemm_trit_matches_gemv():
     planes, _ = synth.trit_planes(N, K, seed=41)
     q, xs = _acts(B, K, seed=42)
     acc, y = gemm_trit(planes, 0.02, q, xs)
-    yv = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
-    av = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    yv = guarded((B, N), torch.float32, float("nan"))
+    av = guarded((B, N), torch.int32)
     lb.lb_gemv_trit_planes(dev(planes), 0.02, dev(q), dev(xs), yv, av, N, K, B)
     torch.cuda.synchronize()
     assert np.array_equal(acc, host(av))
@@ -112,7 +111,7 @@ def test_gemm_trit_workspace_reused():
     N, K = 200, 2048
     planes, _ = synth.trit_planes(N, K, seed=51)
     pd = dev(planes)
-    ws = torch.empty(lb.lb_gemm_trit_workspace_bytes(300, K), dtype=torch.uint8, device="cuda")
+    ws = guarded(lb.lb_gemm_trit_workspace_bytes(300, K), torch.uint8)
     for M, seed in ((300, 52), (77, 53), (300, 54)):
         q, xs = _acts(M, K, seed=seed)
         _check_exact(planes, 0.011, q, xs, workspace=ws, planes_dev=pd)
@@ -124,13 +123,13 @@ def test_gemm_trit_grouped():
     single-matrix call."""
     M, K, Ns = 130, 1216, (130, 1, 257)
     q, xs = _acts(M, K, seed=60)
-    ws = torch.empty(lb.lb_gemm_trit_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    ws = guarded(lb.lb_gemm_trit_workspace_bytes(M, K), torch.uint8)
     mats, outs = [], []
     for i, n in enumerate(Ns):
         planes, _ = synth.trit_planes(n, K, seed=61 + i)
         w = synth.w_scale(70 + i)
-        y = torch.full((M, n), float("nan"), dtype=torch.float32, device="cuda")
-        acc = torch.empty((M, n), dtype=torch.int32, device="cuda") if i != 1 else None
+        y = guarded((M, n), torch.float32, float("nan"))
+        acc = guarded((M, n), torch.int32) if i != 1 else None
         mats.append((dev(planes), w, y, acc, n))
         outs.append((planes, w, y, acc))
     lb.lb_gemm_trit_planes_grouped(mats, dev(q), dev(xs), M, K, ws)

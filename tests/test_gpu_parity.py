@@ -13,7 +13,7 @@ import torch
 import bit_matvec_lb_gb300 as lb
 import oracle
 import synth
-from gpu_util import dev, gemv_bf16, gemv_q, gemv_trit, host, repack_on_gpu, within
+from gpu_util import dev, gemv_bf16, gemv_q, gemv_trit, guarded, host, repack_on_gpu, within
 
 pytestmark = pytest.mark.gpu
 
@@ -32,8 +32,8 @@ def test_quantize_q8_0(B, K):
     if K >= 64:
         x[0, 32:64] *= 1e4                              # a large block
     q_ref, d_ref = oracle.quantize_q8_0(x)
-    q = torch.empty((B, K), dtype=torch.int8, device="cuda")
-    d = torch.empty((B, K // 32), dtype=torch.int16, device="cuda")
+    q = guarded((B, K), torch.int8)
+    d = guarded((B, K // 32), torch.int16)
     lb.lb_quantize_q8_0(dev(x), q, d, B, K)
     torch.cuda.synchronize()
     assert np.array_equal(host(q), q_ref)
@@ -44,8 +44,8 @@ def test_quantize_q8_0_ties():
     from golden_io import read
     gd = read("q8_0_ties.txt")
     x = np.array([[float(t) for t in gd["x"].split()]], dtype=np.float32)
-    q = torch.empty((1, 32), dtype=torch.int8, device="cuda")
-    d = torch.empty((1, 1), dtype=torch.int16, device="cuda")
+    q = guarded((1, 32), torch.int8)
+    d = guarded((1, 1), torch.int16)
     lb.lb_quantize_q8_0(dev(x), q, d, 1, 32)
     torch.cuda.synchronize()
     assert host(q)[0].tolist() == [int(t) for t in gd["q"].split()]
@@ -58,8 +58,8 @@ def test_quantize_i8_absmax(B, K):
     if B > 1:
         x[1] = 0.0
     q_ref, s_ref = oracle.quantize_i8_absmax(x)
-    q = torch.empty((B, K), dtype=torch.int8, device="cuda")
-    s = torch.empty((B,), dtype=torch.float32, device="cuda")
+    q = guarded((B, K), torch.int8)
+    s = guarded((B,), torch.float32)
     lb.lb_quantize_i8_absmax(dev(x), q, s, B, K)
     torch.cuda.synchronize()
     assert np.array_equal(host(q), q_ref)
@@ -205,7 +205,7 @@ def test_q2_4096_batch8_sampled(G):
     mats, ys = [], []
     for i in range(G):
         bits, scales = reps[0] if i < G - 1 or G == 1 else reps[-1]
-        y = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
+        y = guarded((B, N), torch.float32, float("nan"))
         mats.append((bits, scales, y, None, N))
         ys.append(y)
     lb.lb_gemv_q2_0_g64_grouped(mats, dev(q), dev(dx), K, B)
@@ -242,8 +242,8 @@ def test_trit_bitnet_shapes(name, N, K, B):
     """BitNet-2B4T projections, int8 per-token absmax activations (quantized on the GPU)."""
     planes, _ = synth.trit_planes(N, K, seed=700 + N + K)
     x = synth.activations(B, K, seed=701)
-    qd = torch.empty((B, K), dtype=torch.int8, device="cuda")
-    sd = torch.empty((B,), dtype=torch.float32, device="cuda")
+    qd = guarded((B, K), torch.int8)
+    sd = guarded((B,), torch.float32)
     lb.lb_quantize_i8_absmax(dev(x), qd, sd, B, K)
     torch.cuda.synchronize()
     q_ref, s_ref = oracle.quantize_i8_absmax(x)
@@ -301,8 +301,8 @@ def test_grouped_q(qk, B):
     mats, outs = [], []
     for i, (n, bl) in enumerate(zip(Ns, blocks)):
         bits, scales = repack_on_gpu(bl, K, qk)
-        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
-        isum = torch.empty((B, n, K // 32), dtype=torch.int32, device="cuda") if i % 2 else None
+        y = guarded((B, n), torch.float32, float("nan"))
+        isum = guarded((B, n, K // 32), torch.int32) if i % 2 else None
         mats.append((bits, scales, y, isum, n))
         outs.append((y, isum))
     fn = lb.lb_gemv_q1_0_grouped if qk == 128 else lb.lb_gemv_q2_0_g64_grouped
@@ -326,7 +326,7 @@ def test_grouped_q2_full_group():
     mats, ys = [], []
     for n, bl in zip(Ns, blocks):
         bits, scales = repack_on_gpu(bl, K, 64)
-        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
+        y = guarded((B, n), torch.float32, float("nan"))
         mats.append((bits, scales, y, None, n))
         ys.append(y)
     lb.lb_gemv_q2_0_g64_grouped(mats, dev(q), dev(dx), K, B)
@@ -355,8 +355,8 @@ def test_grouped_trit(B):
     xs = (np.abs(synth.activations(1, B, seed=3101)[0]) * 0.01 + 1e-3).astype(np.float32)
     mats, outs = [], []
     for i, (n, pl) in enumerate(zip(Ns, planes)):
-        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
-        acc = torch.empty((B, n), dtype=torch.int32, device="cuda") if i != 1 else None
+        y = guarded((B, n), torch.float32, float("nan"))
+        acc = guarded((B, n), torch.int32) if i != 1 else None
         mats.append((dev(pl), 0.01 * (i + 1), y, acc, n))
         outs.append((y, acc, 0.01 * (i + 1)))
     lb.lb_gemv_trit_planes_grouped(mats, dev(q), dev(xs), K, B)
@@ -430,7 +430,7 @@ def _q_group(qk, Ns, K, B, seed):
     per_bits, per_sc = K // qk * 16, lb.scale_stride(K, qk)
     mats, outs, r0 = [], [], 0
     for n in Ns:
-        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
+        y = guarded((B, n), torch.float32, float("nan"))
         mats.append((bits[r0 * per_bits:(r0 + n) * per_bits], scales[r0 * per_sc:(r0 + n) * per_sc],
                      y, None, n))
         outs.append((blocks[r0:r0 + n], y))
@@ -466,8 +466,8 @@ def test_trit_batched_tensor_core(B):
     qi, xs = oracle.quantize_i8_absmax(x)
     mats, outs, r0 = [], [], 0
     for n in Ns:
-        y = torch.full((B, n), float("nan"), dtype=torch.float32, device="cuda")
-        acc = torch.empty((B, n), dtype=torch.int32, device="cuda")
+        y = guarded((B, n), torch.float32, float("nan"))
+        acc = guarded((B, n), torch.int32)
         mats.append((dev(planes[r0:r0 + n]), 0.0173, y, acc, n))
         outs.append((planes[r0:r0 + n], y, acc))
         r0 += n

@@ -53,6 +53,8 @@ MUTANTS = [
     ("base3_high_digit_first", "int j = (int)((col % 80) / 5), i = (int)(col % 5);",
      "int j = (int)((col % 80) / 5), i = 4 - (int)(col % 5);"),
     ("base3_group_of_64", "int64_t g = col / 80;", "int64_t g = col / 64;"),
+    ("q_mag_signed", "m += fabs(term);", "m += term;"),
+    ("q_mag_without_isum", "m += fabs(term);", "m += fabs((double)dw * (double)dxf) * 32.0 * 128.0;"),
 ]
 
 

@@ -185,6 +185,9 @@ def test_q1_0_brute_force(N, K, B):
             e = sum(Fraction(dw[n, j // 4]) * Fraction(dxf[b, j]) * int(isum[b, n, j])
                     for j in range(K // 32))
             assert Fraction(r.y_exact[b, n]) == e or abs(float(e) - r.y_exact[b, n]) <= 1e-15 * max(1.0, abs(float(e)))
+    # the tolerance magnitude: sum over q8_0 blocks of |d_w * d_x * isum|, from the dense decode
+    mag = np.abs(np.repeat(dw, 4, axis=1)[None, :, :] * dxf[:, None, :] * isum).sum(-1)
+    assert np.allclose(r.mag, mag, rtol=1e-13, atol=0)
 
 
 def test_q1_0_all_ones_identity():
@@ -244,6 +247,9 @@ def test_q2_0_brute_force(N, K, B, probs):
     dw = np.repeat(_f16(_scales(blocks)), 2, axis=1)                   # per q8 block
     expect = np.einsum("nj,bnj->bn", dw, _f16(dx)[:, None, :] * isum)
     assert np.allclose(r.y_exact, expect, rtol=1e-12, atol=1e-300)
+    # the tolerance magnitude: sum over q8_0 blocks of |d_w * d_x * isum|, from the dense decode
+    mag = np.abs(dw[None, :, :] * _f16(dx)[:, None, :] * isum).sum(-1)
+    assert np.allclose(r.mag, mag, rtol=1e-13, atol=0)
 
 
 @pytest.mark.parametrize("code,factor", [(1, 0), (2, 1), (0, -1), (3, 2)])

@@ -27,17 +27,18 @@ def test_noalloc_refuses_oversize_and_null_on_host():
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_two_calls():
     import torch
-    from gpu_util import dev, repack_on_gpu, within
+    from gpu_util import dev, guarded, repack_on_gpu, within
 
     results = []
-    for (M, N, K, seed) in ((130, 300, 2048, 1), (512, 4096, 4096, 2)):
+    # the last shape fills the scratch exactly: round_up(512, 128) * 8192 * 2 B = 8 MiB
+    for (M, N, K, seed) in ((130, 300, 2048, 1), (512, 4096, 4096, 2), (512, 640, 8192, 3)):
         blocks = synth.q2_0_blocks(N, K, seed=900 + seed)
         bits, scales = repack_on_gpu(blocks, K, 64)
         q, dx = oracle.quantize_q8_0(synth.activations(M, K, seed=910 + seed))
         qd, dd = dev(q), dev(dx)
-        y0 = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-        y1 = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-        ws = torch.empty(lb.lb_gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+        y0 = guarded((M, N), torch.float32, float("nan"))
+        y1 = guarded((M, N), torch.float32, float("nan"))
+        ws = guarded(lb.lb_gemm_workspace_bytes(M, K), torch.uint8)
         lb.lb_gemm_q2_0_g64(bits, scales, qd, dd, y0, M, N, K, ws)
         lb.lb_gemm_q2_0_g64_noalloc(bits, scales, qd, dd, y1, M, N, K)
         torch.cuda.synchronize()
