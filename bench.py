@@ -460,6 +460,55 @@ def rows_decode(lb, rows, stream):
     import synth
     hbm, _ = peaks()
 
+    # (0) one token, the other two formats: 64 distinct 4096 x 4096 matrices per grouped launch
+    #     (rotated past L2), quantizer + GEMV per step, beside the Q2_0_g64 headline
+    probe = read_probe(stream)
+    N, K = ROWS_N, ROWS_K
+    x1 = torch.from_numpy(synth.activations(1, K, seed=1)).cuda()
+    q1 = torch.empty((1, K), dtype=torch.int8, device="cuda")
+    d1 = torch.empty((1, K // 32), dtype=torch.int16, device="cuda")
+    s1 = torch.empty((1,), dtype=torch.float32, device="cuda")
+    Y1 = torch.empty((N_ROT, 1, N), dtype=torch.float32, device="cuda")
+    for fmt in ("q1_0", "planar"):
+        if fmt == "q1_0":
+            W1 = [make_q1_weights(N, K, 51_000 + r) for r in range(N_ROT)]
+            wbytes = q1_bytes(N, K)
+            grp = [(W1[r][0], W1[r][1], Y1[r], None, N) for r in range(N_ROT)]
+
+            def quant():
+                lb.lb_quantize_q8_0(x1, q1, d1, 1, K, stream=stream)
+
+            def gemv():
+                lb.lb_gemv_q1_0_grouped(grp, q1, d1, K, 1, stream=stream)
+            act = K + K // 16
+        else:
+            W1 = [synth.device_trit_planes(N, K, 52_000 + r) for r in range(N_ROT)]
+            wbytes = N * K // 64 * 16
+            grp = [(W1[r], 0.02, Y1[r], None, N) for r in range(N_ROT)]
+
+            def quant():
+                lb.lb_quantize_i8_absmax(x1, q1, s1, 1, K, stream=stream)
+
+            def gemv():
+                lb.lb_gemv_trit_planes_grouped(grp, q1, s1, K, 1, stream=stream)
+            act = K + 4
+
+        def step1():
+            quant()
+            gemv()
+        ms = time_graph(Graph(step1, stream), reps=50)
+        ms_g = time_graph(Graph(gemv, stream), reps=50)
+        gbs = N_ROT * wbytes / (ms * 1e-3) / 1e9
+        launch = (N_ROT * (wbytes + 4 * N) + act) / (ms_g * 1e-3) / 1e9
+        rows[f"{fmt}_4096x4096_b1"] = {
+            "GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
+            "launch_GB/s": round(launch, 1), "launch_pct_hbm": round(100 * launch / hbm, 1),
+            "launch_frac_of_read_probe": (round(launch / probe["GB/s"], 4)
+                                          if "GB/s" in probe else None),
+            "weights_per_step": f"{N_ROT} distinct {N}x{K} matrices, {N_ROT * wbytes} B"}
+        del W1, grp
+        torch.cuda.empty_cache()
+
     # (1) config 2 at batch 8
     N, K, B = ROWS_N, ROWS_K, 8
     W = [make_q2_weights(N, K, 50_000 + r) for r in range(N_ROT)]

@@ -23,11 +23,13 @@
 //     fp32.  Each 32-wide block is drained separately (d_x changes every 32 columns of K): the
 //     drain warps read the accumulator with tcgen05.ld and add d_x * (d_w * isum) with one FFMA
 //     per element into registers, flushing to y every 32 blocks, so the fp32 accumulation depth
-//     stays below 32 + K/1024.  Two accumulators alternate so MMAs overlap the drain.
+//     stays below 32 + K/1024.  Four 128-column accumulators (a stage's two K32 steps use two)
+//     let the MMAs of the next stage run while the drain reads the previous one.
 //   * Warp roles in a 512-thread CTA: warps 0-3 expand weights (one row each), warp 4 copies
-//     activation tiles, warp 5 owns tensor memory and issues the MMAs (one thread), warps 8-15
-//     (two warpgroups) drain.  A 4-stage shared-memory ring of {A tile, B tile} decouples them;
-//     every wait is bounded and reports through the device error word.
+//     activation tiles, warps 5 and 6 issue the MMAs (one thread each, alternate stages; warp 5
+//     owns tensor memory), warps 8-15 (two warpgroups) drain.  A 4-stage shared-memory ring of
+//     {two A tiles, two B tiles} decouples them; every wait is bounded and reports through the
+//     device error word.
 #include <algorithm>
 
 #include "lb_tc.cuh"
@@ -290,25 +292,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_q_kernel(const __grid_co
             }
         }
     } else if (warp == 4) {
-        // ---------------- activation tiles: one 16 KB bulk copy per stage ----------------
+        // ---------------- activation tiles: two 8 KB bulk copies per stage ----------------
+        // One thread's bulk copies are served one after another (about 370 clk each, whatever
+        // their size up to 32 KB), so the stage's two tiles are issued by two lanes.
         pdl_wait();
-        if (lane == 0) {
-            const uint8_t *src = p.ws + (int64_t)m_tile * nK32 * kTileBytes;
-            Ring<kStages> rs;
-            int issued = 0;
-            for (int st = 0; st < nst; st++) {
-                if (!wait_or_report(&empty[rs.idx], rs.phase ^ 1u, p.err)) break;
-                mbar_arrive_expect_tx(&full[rs.idx], 2 * kTileBytes);
-                bulk_g2s(gsm + rs.idx * kStageBytes, src + (int64_t)st * 2 * kTileBytes,
-                         2 * kTileBytes, &full[rs.idx]);
-                rs.next();
-                issued = st + 1;
+        const uint8_t *src = p.ws + ((int64_t)m_tile * nK32 + lane) * kTileBytes;
+        Ring<kStages> rs;
+        int issued = 0;
+        for (int st = 0; st < nst; st++) {
+            bool ok = true;
+            if (lane == 0) {
+                ok = wait_or_report(&empty[rs.idx], rs.phase ^ 1u, p.err);
+                if (ok) mbar_arrive_expect_tx(&full[rs.idx], 2 * kTileBytes);
             }
-            // No copy may still be landing in shared memory when the CTA exits: wait for the
-            // stages issued last (immediate on the normal path, bounded on an error path).
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (lane < 2)
+                bulk_g2s(gsm + rs.idx * kStageBytes + lane * kTileBytes,
+                         src + (int64_t)st * 2 * kTileBytes, kTileBytes, &full[rs.idx]);
+            rs.next();
+            issued = st + 1;
+        }
+        // No copy may still be landing in shared memory when the CTA exits: wait for the
+        // stages issued last (immediate on the normal path, bounded on an error path).
+        if (lane == 0)
             for (int st = max(0, issued - kStages); st < issued; st++)
                 mbar_wait(&full[st % kStages], (st / kStages) & 1);
-        }
     } else if (warp >= 5 && warp < 5 + kIssuers) {
         // ---------------- MMA issue: warp 5 + i issues the stages st = i (mod 2) ----------------
         // Issuer i owns accumulators 2i and 2i + 1 (steps 2st and 2st + 1).
@@ -557,29 +565,44 @@ int gemm_q_with_workspace(int q2, const uint8_t *bits, const uint16_t *scales, c
 // GPU design.  Activations are the same f16 operand tiles as the Q1_0 GEMM (its prologue and
 // K permutation); weights are expanded in shared memory to f16 -1 / 0 / +1.  Every partial sum
 // of the tensor core is an integer of magnitude at most 128 K < 2^24, exact in the binary32
-// accumulator whatever the order of the additions, so one tensor-memory accumulator runs over
+// accumulator whatever the order of the additions, so each tensor-memory accumulator runs over
 // the whole of K and is read once at the end: no per-block drain.  For the same reason K may
 // be split across CTAs with no effect on the result: a call whose tiles would leave SMs idle
 // runs the ks splits of each tile as one thread-block cluster; every split parks its integer
-// partial tile in its own shared memory, and after a cluster barrier each CTA adds 1/ks of the
-// tile's columns over the whole cluster (distributed shared memory) and writes those outputs.
-//   Warp roles in a 192-thread CTA (two CTAs per SM): warps 0-3 expand weights (thread = weight
-//   row) and then read the accumulator out (thread = token = tensor-memory lane), warp 4 copies
-//   activation tiles, warp 5 owns tensor memory and issues the MMAs.  Three stages of one
-//   64-column beat each; every mbarrier wait is bounded and reports through the device error
-//   word.  The two cluster barriers are reached by every thread of every CTA on every path.
+// partial tiles in its own shared memory, and after a cluster barrier the CTAs add the partials
+// of their share of the rows over the whole cluster (distributed shared memory).
+//   Tile: 256 tokens (two 128-token tensor-memory accumulators) x 256 weight rows, one
+//   M = 128, N = 256 MMA per token tile and 16-deep step.  Shared-memory bandwidth bounds this
+//   kernel (the tensor core reads both operands from it, and the copies and the weight expansion
+//   write it): N = 256 MMAs read a quarter fewer operand bytes per product than N = 128 ones, and
+//   one activation tile feeds 256 weight rows, one expanded weight tile 256 tokens.
+//   Warp roles in a 320-thread CTA (one per SM): warps 0-7 expand weights (thread = weight row)
+//   and then read the accumulators out, warp 8 copies activation tiles (one 8 KB bulk copy per
+//   lane: one thread's copies are served one after another), warp 9 owns tensor memory and
+//   issues the MMAs.  Three stages of one 64-column beat each; every mbarrier wait is bounded
+//   and reports through the device error word.  Every barrier of the output phase is reached
+//   by every thread of every CTA the same number of times.
 // ==========================================================================================
 namespace lb {
 
-constexpr int kTritThreads = 192;
+constexpr int kTritExpWarps = 8;          // warps 0-7: weight expanders, then the output
+constexpr int kTritCopyWarp = 8;           // activation copies
+constexpr int kTritMmaWarp = 9;            // MMA issue, tensor memory
+constexpr int kTritThreads = 320;
+constexpr int kTritTileN = 256;            // weight rows per tile (one N = 256 MMA)
 constexpr int kTritStages = 3;
-constexpr int kTritSmem = kTritStages * kStageBytes + 1024;
-constexpr int kTritSplitCtas = 304;        // split K while fewer CTAs than this would run
-constexpr int kTritMaxSplit = 4;           // cluster size (portable limit: 8)
+// A stage: the two 32-deep activation tiles of each of the CTA's two token tiles (8 KB each),
+// then the two 256-row expanded weight tiles they share (16 KB each).
+constexpr int kTritBTileBytes = kTritTileN * 32 * 2;
+constexpr int kTritAOffBytes = 4 * kTileBytes;
+constexpr int kTritStageBytes = kTritAOffBytes + 2 * kTritBTileBytes;
+constexpr int kTritSmem = kTritStages * kTritStageBytes + 1024;
+constexpr int kTritSplitCtas = 152;        // split K while fewer CTAs than this would run
+constexpr int kTritMaxSplit = 4;           // cluster size (8 measured slower)
 constexpr int kTritMinStages = 4;          // beats per split, at least
 constexpr int kPartPitch = kTileN + 4;     // partial tile [m][n] row pitch (conflict-free)
-static_assert(kTileM * kPartPitch * 4 <= kTritStages * kStageBytes,
-              "the partial tile must fit in the stage ring");
+static_assert(2 * kTileM * kPartPitch * 4 <= kTritStages * kTritStageBytes,
+              "the partial tiles must fit in the stage ring");
 
 struct TritGemmMat {
     const uint4 *planes;     // [N][K/64] beats {pos lo, pos hi, neg lo, neg hi}
@@ -594,7 +617,7 @@ struct TritGemmParams {
     const uint8_t *ws;       // activation tiles [mtiles][K/32][8192 B]
     const float *x_scale;    // [M]
     int *err;
-    int G, M, nst, mtiles, ks, sps;
+    int G, M, nst, mtiles, mpairs, ks, sps;
 };
 
 // Half a planar beat -- pos word P and neg word Nn of 32 columns, bit c <-> column c -- as the
@@ -628,100 +651,48 @@ __device__ __forceinline__ void expand_trit(uint32_t P, uint32_t Nn, uint4 (&c)[
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
-// Sixteen consecutive floats (16-byte aligned) of CTA `rank`'s shared memory, at the address
-// this CTA uses for them: four loads issued back to back.  Ordered after the cluster barrier
-// as a volatile statement; no memory clobber, so the loads of several ranks can be in flight
-// together.
-__device__ __forceinline__ void ld_cluster16(const float *local, uint32_t rank, float (&o)[16]) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)),
-                 "r"(rank));
-    asm volatile(
-        "ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%16];\n\t"
-        "ld.shared::cluster.v4.f32 {%4, %5, %6, %7}, [%16 + 16];\n\t"
-        "ld.shared::cluster.v4.f32 {%8, %9, %10, %11}, [%16 + 32];\n\t"
-        "ld.shared::cluster.v4.f32 {%12, %13, %14, %15}, [%16 + 48];"
-        : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3]), "=f"(o[4]), "=f"(o[5]), "=f"(o[6]),
-          "=f"(o[7]), "=f"(o[8]), "=f"(o[9]), "=f"(o[10]), "=f"(o[11]), "=f"(o[12]),
-          "=f"(o[13]), "=f"(o[14]), "=f"(o[15])
-        : "r"(remote));
-}
-
-// The W outputs of token row m (yrow / arow point at its row) for weight rows nb .. nb + W - 1,
-// from their exact integer accumulators a[].
-template <int W>
-__device__ __forceinline__ void trit_store(const float (&a)[W], float xs, float w_scale,
-                                           float *yrow, int32_t *arow, int64_t nb, int N) {
-    float o[W];
-#pragma unroll
-    for (int j = 0; j < W; j++) o[j] = __fmul_rn(__fmul_rn(a[j], xs), w_scale);
-    if ((N & 3) == 0 && nb + W <= N) {
-#pragma unroll
-        for (int v = 0; v < W / 4; v++)
-            reinterpret_cast<float4 *>(yrow + nb)[v] =
-                make_float4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-        if (arow) {
-#pragma unroll
-            for (int v = 0; v < W / 4; v++)
-                reinterpret_cast<int4 *>(arow + nb)[v] = make_int4(
-                    __float2int_rn(a[4 * v]), __float2int_rn(a[4 * v + 1]),
-                    __float2int_rn(a[4 * v + 2]), __float2int_rn(a[4 * v + 3]));
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < W; j++) {
-            if (nb + j < N) {
-                yrow[nb + j] = o[j];
-                if (arow) arow[nb + j] = __float2int_rn(a[j]);
-            }
-        }
-    }
-}
-
-__global__ void __launch_bounds__(kTritThreads, 2)
+__global__ void __launch_bounds__(kTritThreads, 1)
     gemm_trit_kernel(const __grid_constant__ TritGemmParams p) {
     extern __shared__ uint8_t gsm_raw[];
     uint8_t *gsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) &
                                                ~(uintptr_t)1023);
-    // full[s]: the stage's two activation tiles have landed and its two weight tiles are written.
-    // empty[s]: the stage's four MMAs have completed (the stage may be refilled).
-    // mma_done: every MMA of the CTA has completed (the accumulator may be read).
+    // full[s]: the stage's activation tiles have landed and its two weight tiles are written.
+    // empty[s]: the stage's MMAs have completed (the stage may be refilled).
+    // mma_done: every MMA of the CTA has completed (the accumulators may be read).
     __shared__ __align__(8) uint64_t full[kTritStages], empty[kTritStages], mma_done;
     __shared__ uint32_t tmem_slot;
+    __shared__ float xs_tile[2 * kTileM];  // activation scales of the tile's tokens
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = (int)blockIdx.x / p.ks, split = (int)blockIdx.x % p.ks;  // split = rank
     int gi = 0;
     while (gi + 1 < p.G && p.mat[gi + 1].tile0 <= tile) gi++;
     const TritGemmMat &W = p.mat[gi];
-    const int m_tile = (tile - W.tile0) % p.mtiles;
-    const int n_tile = (tile - W.tile0) / p.mtiles;
-    const int64_t m0 = (int64_t)m_tile * kTileM, n0 = (int64_t)n_tile * kTileN;
+    // a tile is two token tiles (m_tile, m_tile + 1) x 256 weight rows
+    const int m_pair = (tile - W.tile0) % p.mpairs;
+    const int n_tile = (tile - W.tile0) / p.mpairs;
+    const int m_tile = 2 * m_pair;
+    const int halves = (m_tile + 1 < p.mtiles) ? 2 : 1;  // the last pair may hold one tile
+    const int64_t m0 = (int64_t)m_tile * kTileM, n0 = (int64_t)n_tile * kTritTileN;
     const int sb = split * p.sps;                 // first beat of this split
     const int nloc = min(p.nst, sb + p.sps) - sb;  // beats of this split (>= 1 by construction)
-    float *part = reinterpret_cast<float *>(gsm);  // partial tile, once the ring is idle
+    float *part = reinterpret_cast<float *>(gsm);  // partial tiles, once the ring is idle
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTritStages; s++) {
-            mbar_init(&full[s], 5);   // four expander warps + the activation copy (and its bytes)
-            mbar_init(&empty[s], 1);  // commit after the stage's MMAs
+            mbar_init(&full[s], kTritExpWarps + 1);  // expander warps + the activation copies
+            mbar_init(&empty[s], 1);                 // commit after the stage's MMAs
         }
         mbar_init(&mma_done, 1);
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(&tmem_slot, kTileN);
+    if (warp == kTritMmaWarp) tmem_alloc(&tmem_slot, 2 * kTritTileN);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     pdl_launch_dependents();
 
-    // token row of the epilogue threads (warps 0-3 = tensor-memory lane quarters)
-    const int mrow = threadIdx.x;
-    const int64_t m = m0 + mrow;
-    const bool mvalid = warp < 4 && m < p.M;
-    float xs = 0.f;
-
-    if (warp < 4) {
+    if (warp < kTritExpWarps) {
         // ---------------- weight expanders: thread = weight row ----------------
         // Beats are read kQ stages ahead into a register queue with one fixed slot per stage of
         // the unrolled loop.
@@ -736,7 +707,7 @@ __global__ void __launch_bounds__(kTritThreads, 2)
         uint4 qb[kQ];
 #pragma unroll
         for (int i = 0; i < kQ; i++) qb[i] = load_beat(i);
-        const uint32_t boff = (uint32_t)canon_offset(nl, 0) + 2 * kTileBytes;
+        const uint32_t boff = (uint32_t)canon_offset(nl, 0) + kTritAOffBytes;
         Ring<kTritStages> rs;
         bool ok = true;
         for (int i0 = 0; i0 < nloc && ok; i0 += kQ) {
@@ -749,14 +720,15 @@ __global__ void __launch_bounds__(kTritThreads, 2)
                     ok = false;
                     break;
                 }
-                uint8_t *bt = gsm + rs.idx * kStageBytes + boff;
+                uint8_t *bt = gsm + rs.idx * kTritStageBytes + boff;
 #pragma unroll
                 for (int t = 0; t < 2; t++) {
                     uint4 c[4];
                     expand_trit(t ? qb[j].y : qb[j].x, t ? qb[j].w : qb[j].z, c);
 #pragma unroll
                     for (int kc = 0; kc < 4; kc++)
-                        *reinterpret_cast<uint4 *>(bt + t * kTileBytes + kc * kCoreLBO) = c[kc];
+                        *reinterpret_cast<uint4 *>(bt + t * kTritBTileBytes + kc * kCoreLBO) =
+                            c[kc];
                 }
                 qb[j] = load_beat(i + kQ);
                 fence_proxy_async_smem();
@@ -765,71 +737,60 @@ __global__ void __launch_bounds__(kTritThreads, 2)
                 rs.next();
             }
         }
-
-        // ---------------- accumulator read-out: thread = token (tensor-memory lane) ----------
+        // activation scales of the tile's tokens, for the output phase
         pdl_wait();
-        xs = mvalid ? p.x_scale[m] : 0.f;
-        if (!__all_sync(0xffffffffu, mbar_wait(&mma_done, 0)) && lane == 0) atomicOr(p.err, 1);
-        tc_fence_after();
-        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-        float *yrow = W.y + (mvalid ? m : 0) * (int64_t)W.N;
-        int32_t *arow = W.acc ? W.acc + (mvalid ? m : 0) * (int64_t)W.N : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < kTileN / 32; c++) {
-            uint32_t r[32];
-            __syncwarp();  // the tensor-memory load is warp-collective
-            tmem_ld32(tl + 32 * c, r);
-            if (p.ks > 1) {
-                // every MMA has completed, so the stage ring is idle: park the partial there
-                float4 *dst = reinterpret_cast<float4 *>(part + mrow * kPartPitch + 32 * c);
-#pragma unroll
-                for (int v = 0; v < 8; v++)
-                    dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                         __uint_as_float(r[4 * v + 2]),
-                                         __uint_as_float(r[4 * v + 3]));
-            } else if (mvalid) {
-                float a[32];
-#pragma unroll
-                for (int j = 0; j < 32; j++) a[j] = __uint_as_float(r[j]);
-                trit_store<32>(a, xs, W.w_scale, yrow, arow, n0 + 32 * c, W.N);
-            }
+        if (threadIdx.x < 2 * kTileM) {
+            const int64_t m = m0 + threadIdx.x;
+            xs_tile[threadIdx.x] = (threadIdx.x < halves * kTileM && m < p.M) ? p.x_scale[m] : 0.f;
         }
-    } else if (warp == 4) {
-        // ---------------- activation tiles: one 16 KB bulk copy per stage ----------------
+    } else if (warp == kTritCopyWarp) {
+        // ---------------- activation tiles: one 8 KB bulk copy per tile, lanes in parallel ----
         pdl_wait();
-        if (lane == 0) {
-            const uint8_t *src = p.ws + ((int64_t)m_tile * p.nst + sb) * 2 * kTileBytes;
-            Ring<kTritStages> rs;
-            int issued = 0;
-            for (int i = 0; i < nloc; i++) {
-                if (!wait_or_report(&empty[rs.idx], rs.phase ^ 1u, p.err)) break;
-                mbar_arrive_expect_tx(&full[rs.idx], 2 * kTileBytes);
-                bulk_g2s(gsm + rs.idx * kStageBytes, src + (int64_t)i * 2 * kTileBytes,
-                         2 * kTileBytes, &full[rs.idx]);
-                rs.next();
-                issued = i + 1;
+        const int nt = 2 * halves;                      // tiles per stage
+        const int h = lane >> 1, t = lane & 1;           // this lane's token tile and K32 step
+        const uint8_t *src = p.ws + ((int64_t)(m_tile + h) * p.nst + sb) * 2 * kTileBytes +
+                             (int64_t)t * kTileBytes;
+        Ring<kTritStages> rs;
+        int issued = 0;
+        for (int i = 0; i < nloc; i++) {
+            bool ok = true;
+            if (lane == 0) {
+                ok = wait_or_report(&empty[rs.idx], rs.phase ^ 1u, p.err);
+                if (ok) mbar_arrive_expect_tx(&full[rs.idx], (uint32_t)(nt * kTileBytes));
             }
-            // No copy may still be landing in shared memory when the ring is reused or the CTA
-            // exits.
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (lane < nt)
+                bulk_g2s(gsm + rs.idx * kTritStageBytes + (2 * h + t) * kTileBytes,
+                         src + (int64_t)i * 2 * kTileBytes, kTileBytes, &full[rs.idx]);
+            rs.next();
+            issued = i + 1;
+        }
+        // No copy may still be landing in shared memory when the ring is reused or the CTA
+        // exits.
+        if (lane == 0)
             for (int i = max(0, issued - kTritStages); i < issued; i++)
                 mbar_wait(&full[i % kTritStages], (uint32_t)(i / kTritStages) & 1u);
-        }
-    } else if (warp == 5) {
-        // ---------------- MMA issue: one thread, one accumulator over the split's K ----------
+    } else if (warp == kTritMmaWarp) {
+        // ---------------- MMA issue: one thread, one accumulator per token tile ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kTileM, kTileN);
+            constexpr uint32_t idesc = idesc_f16(kTileM, kTritTileN);
             const uint32_t sbase = smem_u32(gsm);
             Ring<kTritStages> rs;
             for (int i = 0; i < nloc; i++) {
                 if (!wait_or_report(&full[rs.idx], rs.phase, p.err)) break;
                 tc_fence_after();
-                const uint32_t sa = sbase + (uint32_t)(rs.idx * kStageBytes);
+                const uint32_t sa = sbase + (uint32_t)(rs.idx * kTritStageBytes);
 #pragma unroll
                 for (int t = 0; t < 2; t++) {
-                    const uint64_t ad = smem_desc(sa + t * kTileBytes);
-                    const uint64_t bd = smem_desc(sa + (2 + t) * kTileBytes);
-                    mma_f16(tmem, ad, bd, idesc, (i | t) ? 1u : 0u);
-                    mma_f16(tmem, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);
+                    const uint64_t bd = smem_desc(sa + kTritAOffBytes + t * kTritBTileBytes);
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        if (h >= halves) break;
+                        const uint64_t ad = smem_desc(sa + (2 * h + t) * kTileBytes);
+                        const uint32_t d = tmem + (uint32_t)(h * kTritTileN);
+                        mma_f16(d, ad, bd, idesc, (i | t) ? 1u : 0u);
+                        mma_f16(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);
+                    }
                 }
                 mma_commit(&empty[rs.idx]);
                 rs.next();
@@ -839,43 +800,118 @@ __global__ void __launch_bounds__(kTritThreads, 2)
         }
     }
 
-    if (p.ks > 1) {
-        // Split tiles: every CTA of the cluster has parked its partial tile (every thread of
-        // every CTA arrives here once, whatever its role).  CTA `split` then adds the 16-column
-        // chunks c = split, split + ks, ... over the cluster (the loads of all ranks in flight
-        // together) and writes their outputs; the second barrier keeps every partial alive until
-        // all CTAs have read it.
-        __syncwarp();
-        cluster_sync_all();
-        if (warp < 4) {
-            float *yrow = W.y + (mvalid ? m : 0) * (int64_t)W.N;
-            int32_t *arow = W.acc ? W.acc + (mvalid ? m : 0) * (int64_t)W.N : nullptr;
-            for (int c = split; c < kTileN / 16; c += p.ks) {
-                const float *src = part + mrow * kPartPitch + 16 * c;
-                float t[kTritMaxSplit][16];
+    // Output, in two passes of 128 weight rows (the shared memory holds one pass's partials).
+    // Warps 0-7 read the accumulators (warp w: lane quarter w % 4 of token tile w / 4) and park
+    // them in the idle stage ring as [token][column] tiles; then every CTA of the cluster (one CTA
+    // when K is not split) has its partials parked.  Rows are dealt to the ks CTAs in turn; a
+    // warp writes one whole 128-column row per step, lane l taking columns 4l .. 4l + 3
+    // (coalesced 512-byte stores), after adding the ks partials of that row over the cluster
+    // through distributed shared memory.  Integer partials: every sum is an integer below 2^24,
+    // exact in any order; y takes the two roundings of the planar GEMV.  The barriers are reached
+    // by every thread of every CTA the same number of times, whatever its role.
+    if (warp < kTritExpWarps) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&mma_done, 0)) && lane == 0) atomicOr(p.err, 1);
+        tc_fence_after();
+    }
+    for (int pass = 0; pass < 2; pass++) {
+        const int64_t nbase = n0 + pass * kTileN;
+        if (warp < kTritExpWarps) {
+            const int h = warp >> 2, q = warp & 3;
+            if (h < halves) {
+                const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) +
+                                    (uint32_t)(h * kTritTileN + pass * kTileN);
+                const int row = h * kTileM + q * 32 + lane;
+#pragma unroll 1
+                for (int c = 0; c < kTileN / 32; c++) {
+                    uint32_t r[32];
+                    __syncwarp();  // the tensor-memory load is warp-collective
+                    tmem_ld32(tl + 32 * c, r);
+                    float4 *dst = reinterpret_cast<float4 *>(part + row * kPartPitch + 32 * c);
 #pragma unroll
-                for (int s = 0; s < kTritMaxSplit; s++)
-                    if (s < p.ks) ld_cluster16(src, (uint32_t)s, t[s]);
-                // integer partials: every sum stays an integer below 2^24, exact in any order
-                float a[16];
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    a[j] = t[0][j];
-#pragma unroll
-                    for (int s = 1; s < kTritMaxSplit; s++)
-                        if (s < p.ks) a[j] += t[s][j];
+                    for (int v = 0; v < 8; v++)
+                        dst[v] = make_float4(__uint_as_float(r[4 * v]),
+                                             __uint_as_float(r[4 * v + 1]),
+                                             __uint_as_float(r[4 * v + 2]),
+                                             __uint_as_float(r[4 * v + 3]));
                 }
-                if (mvalid) trit_store<16>(a, xs, W.w_scale, yrow, arow, n0 + 16 * c, W.N);
             }
         }
         __syncwarp();
-        cluster_sync_all();
+        if (p.ks > 1)
+            cluster_sync_all();
+        else
+            __syncthreads();
+        if (warp < kTritExpWarps && nbase < W.N) {
+            const int nrows = halves * kTileM;
+            const int64_t nb = nbase + 4 * lane;
+            const bool full4 = (W.N & 3) == 0 && nb + 4 <= W.N;
+            for (int rr = split * kTritExpWarps + warp; rr < nrows;
+                 rr += kTritExpWarps * p.ks) {
+                const int64_t m = m0 + rr;
+                if (m >= p.M) break;  // rows run upward: the rest of the tile is past M as well
+                const float *src = part + rr * kPartPitch + 4 * lane;
+                float4 a = *reinterpret_cast<const float4 *>(src);
+                if (p.ks > 1) {
+                    const uint32_t local = smem_u32(src);
+                    float4 t[kTritMaxSplit];
+#pragma unroll
+                    for (int s = 0; s < kTritMaxSplit; s++) {
+                        t[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (s < p.ks && s != split) {
+                            uint32_t remote;
+                            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                                         : "=r"(remote) : "r"(local), "r"((uint32_t)s));
+                            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                         : "=f"(t[s].x), "=f"(t[s].y), "=f"(t[s].z),
+                                           "=f"(t[s].w)
+                                         : "r"(remote));
+                        }
+                    }
+#pragma unroll
+                    for (int s = 0; s < kTritMaxSplit; s++) {
+                        a.x += t[s].x;
+                        a.y += t[s].y;
+                        a.z += t[s].z;
+                        a.w += t[s].w;
+                    }
+                }
+                const float xs = xs_tile[rr];
+                const float av[4] = {a.x, a.y, a.z, a.w};
+                float o[4];
+#pragma unroll
+                for (int j = 0; j < 4; j++) o[j] = __fmul_rn(__fmul_rn(av[j], xs), W.w_scale);
+                float *yrow = W.y + m * (int64_t)W.N;
+                int32_t *arow = W.acc ? W.acc + m * (int64_t)W.N : nullptr;
+                if (full4) {
+                    *reinterpret_cast<float4 *>(yrow + nb) = make_float4(o[0], o[1], o[2], o[3]);
+                    if (arow)
+                        *reinterpret_cast<int4 *>(arow + nb) =
+                            make_int4(__float2int_rn(av[0]), __float2int_rn(av[1]),
+                                      __float2int_rn(av[2]), __float2int_rn(av[3]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        if (nb + j < W.N) {
+                            yrow[nb + j] = o[j];
+                            if (arow) arow[nb + j] = __float2int_rn(av[j]);
+                        }
+                    }
+                }
+            }
+        }
+        // every partial read before the next pass overwrites it (and, split, before any CTA of
+        // the cluster exits)
+        __syncwarp();
+        if (p.ks > 1)
+            cluster_sync_all();
+        else
+            __syncthreads();
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kTritMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTileN);
+        tmem_dealloc(tmem, 2 * kTritTileN);
     }
 }
 
@@ -889,6 +925,7 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
         return LB_ERR_SHAPE;
     if (workspace_bytes < lb_gemm_workspace_bytes(M, K)) return LB_ERR_SHAPE;
     const int64_t mtiles = (M + kTileM - 1) / kTileM;
+    const int64_t mpairs = (mtiles + 1) / 2;
     TritGemmParams p{};
     int64_t tiles = 0;
     for (int i = 0; i < G; i++) {
@@ -903,7 +940,7 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
         p.mat[i].w_scale = m.w_scale;
         p.mat[i].N = (int)m.N;
         p.mat[i].tile0 = (int)tiles;
-        tiles += mtiles * ((m.N + kTileN - 1) / kTileN);
+        tiles += mpairs * ((m.N + kTritTileN - 1) / kTritTileN);
         if (tiles > 0x7fffffff / kTritMaxSplit) return LB_ERR_SHAPE;
     }
     const int nst = (int)(K / 64);
@@ -934,6 +971,7 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
     p.M = (int)M;
     p.nst = nst;
     p.mtiles = (int)mtiles;
+    p.mpairs = (int)mpairs;
     p.ks = ks;
     p.sps = sps;
     // The ks splits of a tile are consecutive blocks and form one cluster.

@@ -123,12 +123,11 @@ __device__ __forceinline__ void stage_activations(const int8_t *__restrict__ q,
         uint4 *tok = xp + (int64_t)b * (K / 16);
         tok[quad_slot<F>(c, u0)] = o0;
         tok[quad_slot<F>(c, u0 + 1)] = o1;
-        if (F != kTrit) {
-            const int s = byte_sum_s8(lo.x) + byte_sum_s8(lo.y) + byte_sum_s8(lo.z) +
-                          byte_sum_s8(lo.w) + byte_sum_s8(hi.x) + byte_sum_s8(hi.y) +
-                          byte_sum_s8(hi.z) + byte_sum_s8(hi.w);
-            st[i] = make_float2(f16_bits_to_float(d[i]) * 0.015625f, __int_as_float(-64 * s));
-        }
+        const int s = byte_sum_s8(lo.x) + byte_sum_s8(lo.y) + byte_sum_s8(lo.z) +
+                      byte_sum_s8(lo.w) + byte_sum_s8(hi.x) + byte_sum_s8(hi.y) +
+                      byte_sum_s8(hi.z) + byte_sum_s8(hi.w);
+        st[i] = make_float2(F != kTrit ? f16_bits_to_float(d[i]) * 0.015625f : 0.0f,
+                            __int_as_float(-64 * s));
     }
 }
 
@@ -169,6 +168,29 @@ __device__ __forceinline__ int q2_block_dot(uint32_t w0, uint32_t w1, const uint
     a2 = dp4a_us(w1 & 0x30303030u, av1.z, a2);
     a3 = dp4a_us(w1 & 0xC0C0C0C0u, av1.w, a3);
     return a0 * 64 + (a1 * 16 + (a2 * 4 + a3));
+}
+
+// init + 64 * sum over the 32 columns of pos word P / neg word Nn (bit c <-> column c) of
+// w * q, w = p - n.  The 2-bit value c = 1 + p - n of every column is formed for the even and
+// for the odd columns in one addition each (no carry: c <= 2); field r of byte j of the even
+// word is column 8j + 2r, of the odd word 8j + 2r + 1, and lines up with activation word 2r
+// (even) or 2r + 1 (odd) of the Q1_0 image.  As in q2_block_dot, field r is masked in place
+// (value c * 4^r) and the four dp4a accumulators are recombined exactly; init carries the
+// offset -64 * sum q (sum c*q - sum q = sum w*q).
+__device__ __forceinline__ int trit_word_dot(uint32_t P, uint32_t Nn, const uint4 &a0,
+                                             const uint4 &a1, int init) {
+    constexpr uint32_t M = 0x55555555u;
+    const uint32_t fe = (P & M) + (~Nn & M);
+    const uint32_t fo = ((P >> 1) & M) + ((~Nn >> 1) & M);
+    int s0 = dp4a_us(fe & 0x03030303u, a0.x, 0);
+    int s1 = dp4a_us(fe & 0x0C0C0C0Cu, a0.z, 0);
+    int s2 = dp4a_us(fe & 0x30303030u, a1.x, 0);
+    int s3 = dp4a_us(fe & 0xC0C0C0C0u, a1.z, init);
+    s0 = dp4a_us(fo & 0x03030303u, a0.y, s0);
+    s1 = dp4a_us(fo & 0x0C0C0C0Cu, a0.w, s1);
+    s2 = dp4a_us(fo & 0x30303030u, a1.y, s2);
+    s3 = dp4a_us(fo & 0xC0C0C0C0u, a1.w, s3);
+    return s0 * 64 + (s1 * 16 + (s2 * 4 + s3));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -335,18 +357,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 for (int b = 0; b < B; b++) {
                     const uint4 *tok = xp + b * tok_quads;
                     if (F == kTrit) {
+                        const float2 *stb = st + b * nq8 + cg * 2;
 #pragma unroll
                         for (int h = 0; h < 2; h++) {  // columns 32h .. 32h+31 of the beat
                             const uint4 a0 = tok[quad_slot<F>(cg, 2 * h)];
                             const uint4 a1 = tok[quad_slot<F>(cg, 2 * h + 1)];
+                            const int s64 = __float_as_int(stb[h].y);  // -64 * sum q
 #pragma unroll
                             for (int rr = 0; rr < RW; rr++) {
                                 const uint32_t pw = h ? wv[rr].y : wv[rr].x;
                                 const uint32_t nw = h ? wv[rr].w : wv[rr].z;
-                                // select-accumulate: + where pos, - where neg (x128, exact)
-                                const int vp = q1_word_dot(pw, a0, a1, 0);
-                                const int vn = q1_word_dot(nw, a0, a1, 0);
-                                acc[rr][b] += (Acc)((vp - vn) >> 7);
+                                // select-accumulate: + where pos, - where neg (x64, exact)
+                                acc[rr][b] += (Acc)(trit_word_dot(pw, nw, a0, a1, s64) >> 6);
                             }
                         }
                     } else {
@@ -436,8 +458,7 @@ inline StreamPlan plan_stream(int F, int B, int64_t K, int max_rw) {
     const int scale_b = F == kTrit ? 0 : 2;
     const int budget = 40 * 1024;
     StreamPlan pl{};
-    pl.act_bytes = (int)(((int64_t)B * K + (F == kTrit ? 0 : (int64_t)B * (K / 32) * 8) + 127) /
-                         128 * 128);
+    pl.act_bytes = (int)(((int64_t)B * K + (int64_t)B * (K / 32) * 8 + 127) / 128 * 128);
     int KC = nchunk;
     auto row_cost = [&](int kc) { return kc * 16 + ((kc + 7) & ~7) * scale_b; };
     int RW = 1;
@@ -629,13 +650,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 for (int b = 0; b < B; b++) {
                     const uint4 *tok = xp + b * tok_quads;
                     if (F == kTrit) {
+                        const float2 *stb = st + b * nq8 + cg * 2;
 #pragma unroll
                         for (int h = 0; h < 2; h++) {
                             const uint4 a0 = tok[quad_slot<F>(cg, 2 * h)];
                             const uint4 a1 = tok[quad_slot<F>(cg, 2 * h + 1)];
-                            const int vp = q1_word_dot(h ? wv.y : wv.x, a0, a1, 0);
-                            const int vn = q1_word_dot(h ? wv.w : wv.z, a0, a1, 0);
-                            acc[b] += (Acc)((vp - vn) >> 7);
+                            const int s64 = __float_as_int(stb[h].y);  // -64 * sum q
+                            acc[b] += (Acc)(trit_word_dot(h ? wv.y : wv.x, h ? wv.w : wv.z, a0,
+                                                          a1, s64) >> 6);
                         }
                     } else {
                         const float2 *stb = st + b * nq8 + cg * kPer;
@@ -707,8 +729,7 @@ inline StreamPlan plan_rows(int F, int B, int64_t K, int tr) {
     const int nchunk = (int)(K / cols);
     const int scale_b = F == kTrit ? 0 : 2;
     StreamPlan pl{};
-    pl.act_bytes = (int)(((int64_t)B * K + (F == kTrit ? 0 : (int64_t)B * (K / 32) * 8) + 127) /
-                         128 * 128);
+    pl.act_bytes = (int)(((int64_t)B * K + (int64_t)B * (K / 32) * 8 + 127) / 128 * 128);
     auto stage_cost = [&](int kc) { return tr * ((kc + 1) * 16 + ((kc + 7) & ~7) * scale_b); };
     const int red_b = kConsumerWarps * B * tr * 4;
     // Stage budget: two stages next to the activation image should still let two CTAs share
