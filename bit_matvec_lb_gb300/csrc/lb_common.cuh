@@ -213,22 +213,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     return mbar_wait_slow(bar, parity, limit_ns);
 }
-// Bounded wait for latency-critical hand-offs (tensor-core completion, accumulator release):
-// polls try_wait without a suspend hint -- a suspended thread was measured to resume a few
-// hundred cycles after the phase completed.  Same limit and result as mbar_wait.
-__device__ __noinline__ static bool mbar_spin_slow(uint64_t *bar, uint32_t parity,
-                                                   uint64_t limit_ns) {
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; i++) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) return false;
-    }
-}
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity,
-                                               uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return mbar_spin_slow(bar, parity, limit_ns);
-}
 // 2-D tensor copy (box at column byte x, row y) global -> this CTA's shared memory, counted on
 // `bar`.  x must be a multiple of 16.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,

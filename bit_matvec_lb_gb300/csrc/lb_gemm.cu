@@ -617,7 +617,7 @@ struct TritGemmParams {
     const uint8_t *ws;       // activation tiles [mtiles][K/32][8192 B]
     const float *x_scale;    // [M]
     int *err;
-    int G, M, nst, mtiles, mpairs, ks, sps;
+    int G, M, nst, mtiles, mstep, mpairs, ks, sps;
 };
 
 // Half a planar beat -- pos word P and neg word Nn of 32 columns, bit c <-> column c -- as the
@@ -667,11 +667,11 @@ __global__ void __launch_bounds__(kTritThreads, 1)
     int gi = 0;
     while (gi + 1 < p.G && p.mat[gi + 1].tile0 <= tile) gi++;
     const TritGemmMat &W = p.mat[gi];
-    // a tile is two token tiles (m_tile, m_tile + 1) x 256 weight rows
+    // a tile is p.mstep (1 or 2) token tiles from m_tile on x 256 weight rows
     const int m_pair = (tile - W.tile0) % p.mpairs;
     const int n_tile = (tile - W.tile0) / p.mpairs;
-    const int m_tile = 2 * m_pair;
-    const int halves = (m_tile + 1 < p.mtiles) ? 2 : 1;  // the last pair may hold one tile
+    const int m_tile = p.mstep * m_pair;
+    const int halves = min(p.mstep, p.mtiles - m_tile);  // the last pair may hold one tile
     const int64_t m0 = (int64_t)m_tile * kTileM, n0 = (int64_t)n_tile * kTritTileN;
     const int sb = split * p.sps;                 // first beat of this split
     const int nloc = min(p.nst, sb + p.sps) - sb;  // beats of this split (>= 1 by construction)
@@ -925,7 +925,12 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
         return LB_ERR_SHAPE;
     if (workspace_bytes < lb_gemm_workspace_bytes(M, K)) return LB_ERR_SHAPE;
     const int64_t mtiles = (M + kTileM - 1) / kTileM;
-    const int64_t mpairs = (mtiles + 1) / 2;
+    // Two token tiles per CTA share each expanded weight tile; a call with few tiles takes one
+    // per CTA instead, so that more SMs work on it.
+    int64_t ntiles = 0;
+    for (int i = 0; i < G; i++) ntiles += (mats[i].N + kTritTileN - 1) / kTritTileN;
+    const int mstep = ((mtiles + 1) / 2 * ntiles < kTritSplitCtas / 2) ? 1 : 2;
+    const int64_t mpairs = (mtiles + mstep - 1) / mstep;
     TritGemmParams p{};
     int64_t tiles = 0;
     for (int i = 0; i < G; i++) {
@@ -971,6 +976,7 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
     p.M = (int)M;
     p.nst = nst;
     p.mtiles = (int)mtiles;
+    p.mstep = mstep;
     p.mpairs = (int)mpairs;
     p.ks = ks;
     p.sps = sps;
