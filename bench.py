@@ -1,7 +1,7 @@
 """Benchmark of the GB300 low-bit product library.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
-                    [--rows-only decode|prefill]
+                    [--rows-only stream|decode|prefill]
 
 Headline workload (the decode GEMV the metric is quoted on): Q2_0_g64 GEMV, 4096 x 4096 weights,
 batch 1, q8_0 activations.  One step = one pass of the decode hot path over one token: q8_0
@@ -446,7 +446,10 @@ def rows_measure(lb, out, which: str = "all"):
     import synth
     stream = torch.cuda.Stream()
     rows = {}
+    if which == "stream":
+        rows_stream(lb, rows, stream)
     if which in ("all", "decode"):
+        rows_stream(lb, rows, stream)
         rows_decode(lb, rows, stream)
         rows_dequant(lb, rows, stream)
         rows_base3(lb, rows, stream)
@@ -455,7 +458,7 @@ def rows_measure(lb, out, which: str = "all"):
     out["rows"] = rows
 
 
-def rows_decode(lb, rows, stream):
+def rows_stream(lb, rows, stream):
     import torch
     import synth
     hbm, _ = peaks()
@@ -508,6 +511,12 @@ def rows_decode(lb, rows, stream):
             "weights_per_step": f"{N_ROT} distinct {N}x{K} matrices, {N_ROT * wbytes} B"}
         del W1, grp
         torch.cuda.empty_cache()
+
+
+def rows_decode(lb, rows, stream):
+    import torch
+    import synth
+    hbm, _ = peaks()
 
     # (1) config 2 at batch 8
     N, K, B = ROWS_N, ROWS_K, 8
@@ -810,7 +819,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true")
-    ap.add_argument("--rows-only", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--rows-only", choices=["stream", "decode", "prefill"], default=None,
                     help="skip the headline; run (and print) only these rows")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
