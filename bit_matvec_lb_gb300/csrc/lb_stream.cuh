@@ -170,27 +170,35 @@ __device__ __forceinline__ int q2_block_dot(uint32_t w0, uint32_t w1, const uint
     return a0 * 64 + (a1 * 16 + (a2 * 4 + a3));
 }
 
-// init + 64 * sum over the 32 columns of pos word P / neg word Nn (bit c <-> column c) of
-// w * q, w = p - n.  The 2-bit value c = 1 + p - n of every column is formed for the even and
-// for the odd columns in one addition each (no carry: c <= 2); field r of byte j of the even
-// word is column 8j + 2r, of the odd word 8j + 2r + 1, and lines up with activation word 2r
-// (even) or 2r + 1 (odd) of the Q1_0 image.  As in q2_block_dot, field r is masked in place
-// (value c * 4^r) and the four dp4a accumulators are recombined exactly; init carries the
-// offset -64 * sum q (sum c*q - sum q = sum w*q).
-__device__ __forceinline__ int trit_word_dot(uint32_t P, uint32_t Nn, const uint4 &a0,
-                                             const uint4 &a1, int init) {
+// Adds init + 64 * sum over the 32 columns of pos word P / neg word Nn (bit c <-> column c) of
+// w * q, w = p - n, into four field sums s[0..3].  The 2-bit value c = 1 + p - n of every column
+// is formed for the even and for the odd columns in one addition each (no carry: c <= 2); field
+// r of byte j of the even word is column 8j + 2r, of the odd word 8j + 2r + 1, and lines up with
+// activation word 2r (even) or 2r + 1 (odd) of the Q1_0 image.  As in q2_block_dot, field r is
+// masked in place (value c * 4^r); init carries the offset -64 * sum q (sum c*q - sum q =
+// sum w*q).  With one activation scale per token the sums stay apart for a whole row and
+// trit_combine forms 64 * sum w*q = 64 s[0] + 16 s[1] + 4 s[2] + s[3] once at its end, not once
+// per 32 columns.
+__device__ __forceinline__ void trit_word_acc(uint32_t P, uint32_t Nn, const uint4 &a0,
+                                              const uint4 &a1, int init, int (&s)[4]) {
     constexpr uint32_t M = 0x55555555u;
     const uint32_t fe = (P & M) + (~Nn & M);
     const uint32_t fo = ((P >> 1) & M) + ((~Nn >> 1) & M);
-    int s0 = dp4a_us(fe & 0x03030303u, a0.x, 0);
-    int s1 = dp4a_us(fe & 0x0C0C0C0Cu, a0.z, 0);
-    int s2 = dp4a_us(fe & 0x30303030u, a1.x, 0);
-    int s3 = dp4a_us(fe & 0xC0C0C0C0u, a1.z, init);
-    s0 = dp4a_us(fo & 0x03030303u, a0.y, s0);
-    s1 = dp4a_us(fo & 0x0C0C0C0Cu, a0.w, s1);
-    s2 = dp4a_us(fo & 0x30303030u, a1.y, s2);
-    s3 = dp4a_us(fo & 0xC0C0C0C0u, a1.w, s3);
-    return s0 * 64 + (s1 * 16 + (s2 * 4 + s3));
+    s[0] = dp4a_us(fe & 0x03030303u, a0.x, s[0]);
+    s[1] = dp4a_us(fe & 0x0C0C0C0Cu, a0.z, s[1]);
+    s[2] = dp4a_us(fe & 0x30303030u, a1.x, s[2]);
+    s[3] = dp4a_us(fe & 0xC0C0C0C0u, a1.z, s[3] + init);
+    s[0] = dp4a_us(fo & 0x03030303u, a0.y, s[0]);
+    s[1] = dp4a_us(fo & 0x0C0C0C0Cu, a0.w, s[1]);
+    s[2] = dp4a_us(fo & 0x30303030u, a1.y, s[2]);
+    s[3] = dp4a_us(fo & 0xC0C0C0C0u, a1.w, s[3]);
+}
+// (the weighted sum is formed modulo 2^32: the terms may pass 2^31 while the result, 64 times a
+// dot product of at most 2^17 columns of |q| <= 128, does not)
+__device__ __forceinline__ int trit_combine(const int (&s)[4]) {
+    const uint32_t t = (uint32_t)s[0] * 64u + (uint32_t)s[1] * 16u + (uint32_t)s[2] * 4u +
+                       (uint32_t)s[3];
+    return (int)t >> 6;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -328,10 +336,19 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         const int rows = min(TR, M.N - row0);
         typedef typename std::conditional<F == kTrit, int, float>::type Acc;
         Acc acc[RW][B];
+        int fs[F == kTrit ? RW : 1][F == kTrit ? B : 1][4];  // planar field sums
 #pragma unroll
         for (int rr = 0; rr < RW; rr++)
 #pragma unroll
             for (int b = 0; b < B; b++) acc[rr][b] = 0;
+        if (F == kTrit) {
+#pragma unroll
+            for (int rr = 0; rr < (F == kTrit ? RW : 1); rr++)
+#pragma unroll
+                for (int b = 0; b < (F == kTrit ? B : 1); b++)
+#pragma unroll
+                    for (int f = 0; f < 4; f++) fs[rr][b][f] = 0;
+        }
 
         for (int ct = 0; ct < p.nct; ct++) {
             const int c0 = ct * KC;
@@ -368,7 +385,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                                 const uint32_t pw = h ? wv[rr].y : wv[rr].x;
                                 const uint32_t nw = h ? wv[rr].w : wv[rr].z;
                                 // select-accumulate: + where pos, - where neg (x64, exact)
-                                acc[rr][b] += (Acc)(trit_word_dot(pw, nw, a0, a1, s64) >> 6);
+                                trit_word_acc(pw, nw, a0, a1, s64,
+                                              fs[F == kTrit ? rr : 0][F == kTrit ? b : 0]);
                             }
                         }
                     } else {
@@ -419,6 +437,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
             }
         }
         // finish the rows of this tile
+        if (F == kTrit) {
+#pragma unroll
+            for (int rr = 0; rr < RW; rr++)
+#pragma unroll
+                for (int b = 0; b < B; b++)
+                    acc[rr][b] = (Acc)trit_combine(fs[F == kTrit ? rr : 0][F == kTrit ? b : 0]);
+        }
 #pragma unroll
         for (int rr = 0; rr < RW; rr++) {
             const int r = warp * RW + rr;
@@ -624,8 +649,15 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         const int rows = min(TR, M.N - row0);
         typedef typename std::conditional<F == kTrit, int, float>::type Acc;
         Acc acc[B];
+        int fs[F == kTrit ? B : 1][4];  // planar field sums
 #pragma unroll
         for (int b = 0; b < B; b++) acc[b] = 0;
+        if (F == kTrit) {
+#pragma unroll
+            for (int b = 0; b < (F == kTrit ? B : 1); b++)
+#pragma unroll
+                for (int f = 0; f < 4; f++) fs[b][f] = 0;
+        }
 
         for (int ct = 0; ct < p.nct; ct++) {
             const int c0 = ct * KC;
@@ -656,8 +688,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                             const uint4 a0 = tok[quad_slot<F>(cg, 2 * h)];
                             const uint4 a1 = tok[quad_slot<F>(cg, 2 * h + 1)];
                             const int s64 = __float_as_int(stb[h].y);  // -64 * sum q
-                            acc[b] += (Acc)(trit_word_dot(h ? wv.y : wv.x, h ? wv.w : wv.z, a0,
-                                                          a1, s64) >> 6);
+                            trit_word_acc(h ? wv.y : wv.x, h ? wv.w : wv.z, a0, a1, s64,
+                                          fs[F == kTrit ? b : 0]);
                         }
                     } else {
                         const float2 *stb = st + b * nq8 + cg * kPer;
@@ -685,6 +717,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 stage = 0;
                 phase ^= 1;
             }
+        }
+        if (F == kTrit) {
+#pragma unroll
+            for (int b = 0; b < B; b++) acc[b] = (Acc)trit_combine(fs[F == kTrit ? b : 0]);
         }
         // add the row groups' partial sums (shuffles), then the eight warps' (shared memory)
 #pragma unroll
