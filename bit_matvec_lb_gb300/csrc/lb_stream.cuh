@@ -171,19 +171,21 @@ __device__ __forceinline__ int q2_block_dot(uint32_t w0, uint32_t w1, const uint
 }
 
 // Adds init + 64 * sum over the 32 columns of pos word P / neg word Nn (bit c <-> column c) of
-// w * q, w = p - n, into four field sums s[0..3].  The 2-bit value c = 1 + p - n of every column
-// is formed for the even and for the odd columns in one addition each (no carry: c <= 2); field
-// r of byte j of the even word is column 8j + 2r, of the odd word 8j + 2r + 1, and lines up with
-// activation word 2r (even) or 2r + 1 (odd) of the Q1_0 image.  As in q2_block_dot, field r is
-// masked in place (value c * 4^r); init carries the offset -64 * sum q (sum c*q - sum q =
-// sum w*q).  With one activation scale per token the sums stay apart for a whole row and
-// trit_combine forms 64 * sum w*q = 64 s[0] + 16 s[1] + 4 s[2] + s[3] once at its end, not once
-// per 32 columns.
+// c * q, c = 1 + p - n in {0, 1, 2}, into four field sums s[0..3].  The two bits of c are p
+// (high) and u = not(p or n) (low), so with u formed once the 2-bit values of the even columns
+// are ((P << 1) and odd bits) or (u and even bits), those of the odd columns (P and odd bits) or
+// ((u >> 1) and even bits): field j of the even word is column 2j, of the odd word column 2j + 1,
+// and field r of byte i (column 8i + 2r or 8i + 2r + 1) lines up with activation word 2r (even)
+// or 2r + 1 (odd) of the Q1_0 image.  As in q2_block_dot, field r is masked in place (value
+// c * 4^r) and dp4a-accumulated into s[r]; with one activation scale per token the sums stay
+// apart for a whole row and trit_combine forms (64 s[0] + 16 s[1] + 4 s[2] + s[3]) / 64 once at
+// its end.  init carries the offset -64 * sum q of the word (sum c*q - sum q = sum w*q).
 __device__ __forceinline__ void trit_word_acc(uint32_t P, uint32_t Nn, const uint4 &a0,
                                               const uint4 &a1, int init, int (&s)[4]) {
-    constexpr uint32_t M = 0x55555555u;
-    const uint32_t fe = (P & M) + (~Nn & M);
-    const uint32_t fo = ((P >> 1) & M) + ((~Nn >> 1) & M);
+    constexpr uint32_t E = 0x55555555u;  // bit 2j of every field
+    const uint32_t u = ~(P | Nn);
+    const uint32_t fe = ((P << 1) & ~E) | (u & E);
+    const uint32_t fo = (P & ~E) | ((u >> 1) & E);
     s[0] = dp4a_us(fe & 0x03030303u, a0.x, s[0]);
     s[1] = dp4a_us(fe & 0x0C0C0C0Cu, a0.z, s[1]);
     s[2] = dp4a_us(fe & 0x30303030u, a1.x, s[2]);
@@ -211,6 +213,41 @@ __device__ __forceinline__ int warp_sum_int(int v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Sums each of V per-lane values over the warp with VP - 1 + 5 - log2(VP) shuffles instead of
+// 5 V (VP = V rounded up to a power of two, at most 32).  At the step with lane distance o the
+// lanes with bit o set keep the upper half of the values still held, the others the lower half,
+// and each adds its partner's copy of the half it keeps; then the one value left is summed over
+// the remaining lane bits.  Lane l with l % (32 / VP) == 0 ends with the total of value
+// l / (32 / VP), which the return value carries (values >= V are zero).
+template <int V>
+struct PowTwo {
+    static constexpr int value = V <= 1 ? 1 : V <= 2 ? 2 : V <= 4 ? 4 : V <= 8 ? 8 : V <= 16 ? 16 : 32;
+    static constexpr int log2 = V <= 1 ? 0 : V <= 2 ? 1 : V <= 4 ? 2 : V <= 8 ? 3 : V <= 16 ? 4 : 5;
+};
+template <int V, typename T>
+__device__ __forceinline__ T warp_sum_many(const T (&in)[V], int lane) {
+    static_assert(V >= 1 && V <= 32, "at most 32 values");
+    constexpr int VP = PowTwo<V>::value;
+    T v[VP];
+#pragma unroll
+    for (int i = 0; i < VP; i++) v[i] = i < V ? in[i] : T(0);
+#pragma unroll
+    for (int k = 0; k < PowTwo<V>::log2; k++) {
+        const int o = 16 >> k, n = VP >> k;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; i++) {
+            const T send = up ? v[i] : v[i + n / 2];
+            const T keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+#pragma unroll
+    for (int o = 16 >> PowTwo<V>::log2; o > 0; o >>= 1)
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    return v[0];
 }
 
 // Matrix that owns row tile u, starting the search at `mi` (a CTA visits tiles in increasing
@@ -436,31 +473,29 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                 phase ^= 1;
             }
         }
-        // finish the rows of this tile
-        if (F == kTrit) {
+        // finish the rows of this tile: the RW x B sums over the warp, one lane per result
+        constexpr int V = RW * B;
+        constexpr int kSpan = 32 / PowTwo<V>::value;  // lanes per result after the reduction
+        Acc part[V];
 #pragma unroll
-            for (int rr = 0; rr < RW; rr++)
+        for (int rr = 0; rr < RW; rr++)
 #pragma unroll
-                for (int b = 0; b < B; b++)
-                    acc[rr][b] = (Acc)trit_combine(fs[F == kTrit ? rr : 0][F == kTrit ? b : 0]);
-        }
-#pragma unroll
-        for (int rr = 0; rr < RW; rr++) {
-            const int r = warp * RW + rr;
-#pragma unroll
-            for (int b = 0; b < B; b++) {
-                if (F == kTrit) {
-                    const int a = warp_sum_int((int)acc[rr][b]);
-                    if (lane == 0 && r < rows) {
-                        const int64_t o = (int64_t)b * M.N + row0 + r;
-                        const float t = __fmul_rn((float)a, p.x_scale[b]);
-                        M.y[o] = __fmul_rn(t, M.w_scale);
-                        if (M.aux) M.aux[o] = a;
-                    }
-                } else {
-                    const float v = warp_sum((float)acc[rr][b]);
-                    if (lane == 0 && r < rows) M.y[(int64_t)b * M.N + row0 + r] = v;
-                }
+            for (int b = 0; b < B; b++)
+                part[rr * B + b] =
+                    F == kTrit ? (Acc)trit_combine(fs[F == kTrit ? rr : 0][F == kTrit ? b : 0])
+                               : acc[rr][b];
+        const Acc tot = warp_sum_many<V>(part, lane);
+        const int vi = lane / kSpan;
+        const int r = warp * RW + vi / B, b = vi % B;
+        if (lane % kSpan == 0 && vi < V && r < rows) {
+            const int64_t o = (int64_t)b * M.N + row0 + r;
+            if (F == kTrit) {
+                const int a = (int)tot;
+                const float t = __fmul_rn((float)a, p.x_scale[b]);
+                M.y[o] = __fmul_rn(t, M.w_scale);
+                if (M.aux) M.aux[o] = a;
+            } else {
+                M.y[o] = (float)tot;
             }
         }
     }
