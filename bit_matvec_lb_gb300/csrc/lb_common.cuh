@@ -102,6 +102,29 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
+// Logic operations as single PTX instructions.  The mask-in-place word dots need one logic
+// operation per mask; written in C++ the compiler may distribute a mask over the operation that
+// formed its operand (one operation becomes two), which costs the decode loops about 10 %.
+template <uint32_t M>
+__device__ __forceinline__ uint32_t and_imm(uint32_t a) {
+    uint32_t d;
+    asm("and.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "n"(M));
+    return d;
+}
+// (a and not m) or (b and m)
+template <uint32_t M>
+__device__ __forceinline__ uint32_t select_imm(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xD8;" : "=r"(d) : "r"(a), "r"(b), "n"(M));
+    return d;
+}
+// not (a or b)
+__device__ __forceinline__ uint32_t nor_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, 0, 0x03;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ float f16_bits_to_float(uint16_t h) {
     return __half2float(__ushort_as_half(h));
 }

@@ -183,17 +183,17 @@ __device__ __forceinline__ int q2_block_dot(uint32_t w0, uint32_t w1, const uint
 __device__ __forceinline__ void trit_word_acc(uint32_t P, uint32_t Nn, const uint4 &a0,
                                               const uint4 &a1, int init, int (&s)[4]) {
     constexpr uint32_t E = 0x55555555u;  // bit 2j of every field
-    const uint32_t u = ~(P | Nn);
-    const uint32_t fe = ((P << 1) & ~E) | (u & E);
-    const uint32_t fo = (P & ~E) | ((u >> 1) & E);
-    s[0] = dp4a_us(fe & 0x03030303u, a0.x, s[0]);
-    s[1] = dp4a_us(fe & 0x0C0C0C0Cu, a0.z, s[1]);
-    s[2] = dp4a_us(fe & 0x30303030u, a1.x, s[2]);
-    s[3] = dp4a_us(fe & 0xC0C0C0C0u, a1.z, s[3] + init);
-    s[0] = dp4a_us(fo & 0x03030303u, a0.y, s[0]);
-    s[1] = dp4a_us(fo & 0x0C0C0C0Cu, a0.w, s[1]);
-    s[2] = dp4a_us(fo & 0x30303030u, a1.y, s[2]);
-    s[3] = dp4a_us(fo & 0xC0C0C0C0u, a1.w, s[3]);
+    const uint32_t u = nor_u32(P, Nn);
+    const uint32_t fe = select_imm<E>(P << 1, u);
+    const uint32_t fo = select_imm<E>(P, u >> 1);
+    s[0] = dp4a_us(and_imm<0x03030303u>(fe), a0.x, s[0]);
+    s[1] = dp4a_us(and_imm<0x0C0C0C0Cu>(fe), a0.z, s[1]);
+    s[2] = dp4a_us(and_imm<0x30303030u>(fe), a1.x, s[2]);
+    s[3] = dp4a_us(and_imm<0xC0C0C0C0u>(fe), a1.z, s[3] + init);
+    s[0] = dp4a_us(and_imm<0x03030303u>(fo), a0.y, s[0]);
+    s[1] = dp4a_us(and_imm<0x0C0C0C0Cu>(fo), a0.w, s[1]);
+    s[2] = dp4a_us(and_imm<0x30303030u>(fo), a1.y, s[2]);
+    s[3] = dp4a_us(and_imm<0xC0C0C0C0u>(fo), a1.w, s[3]);
 }
 // (the weighted sum is formed modulo 2^32: the terms may pass 2^31 while the result, 64 times a
 // dot product of at most 2^17 columns of |q| <= 128, does not)
@@ -398,7 +398,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
             const uint4 *sw = reinterpret_cast<const uint4 *>(sb) + warp * RW * KC;
             const uint16_t *ss =
                 reinterpret_cast<const uint16_t *>(sb + (size_t)TR * KC * 16) + warp * RW * KCp;
-            for (int c = lane; c < kc; c += 32) {
+            // one chunk of this lane (every lane takes chunks lane, lane + 32, ...)
+            auto chunk = [&](const int c) {
                 const int cg = c0 + c;  // chunk index within the row
                 uint4 wv[RW];
                 float dw[RW];
@@ -465,6 +466,15 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                             acc[rr][b] = fmaf(dw[rr], t[rr], acc[rr][b]);
                     }
                 }
+            };
+            if ((B == 1 && !AUX) && kc % 64 == 0) {
+                // every lane has the same even number of chunks: two per pass, so that
+                // the loads of one overlap the arithmetic of the other (at one token only;
+                // more tokens would spill registers)
+#pragma unroll 2
+                for (int c = lane; c < kc; c += 32) chunk(c);
+            } else {
+                for (int c = lane; c < kc; c += 32) chunk(c);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
@@ -868,7 +878,24 @@ inline int launch_stream(StreamParams &p, bool aux, int sms, cudaStream_t st) {
     if constexpr (B > 2) {
         return launch_rows<F, B>(p, sms, st);
     } else {
-        const StreamPlan pl = plan_stream(F, B, p.K, 4);
+        // Q1_0 rows are short (a chunk is 128 weights): eight rows per warp cut the fixed cost
+        // per row (stage hand-off, reduction, activation loads) at one token; a 64-row tile
+        // then costs about 7/4 of a 32-row one.  Taken where that wins over whole waves of
+        // tiles on the CTA slots (two per SM).
+        int max_rw = 4;
+        if (F == kQ1 && B == 1) {
+            int64_t t8 = 0, t4 = 0;
+            for (int i = 0; i < p.G; i++) {
+                t8 += (p.m[i].N + 63) / 64;
+                t4 += (p.m[i].N + 31) / 32;
+            }
+            const int64_t slots = 2 * (int64_t)sms;
+            if ((t8 + slots - 1) / slots * 7 < (t4 + slots - 1) / slots * 4) max_rw = 8;
+        }
+        const StreamPlan pl = plan_stream(F, B, p.K, max_rw);
+        if constexpr (F == kQ1 && B == 1) {
+            if (pl.RW == 8) return launch_stream_cfg<F, B, 8, false>(p, pl, sms, st);
+        }
         if (pl.RW == 4) return launch_stream_cfg<F, B, 4, false>(p, pl, sms, st);
         if (pl.RW == 2) return launch_stream_cfg<F, B, 2, false>(p, pl, sms, st);
         return launch_stream_cfg<F, B, 1, false>(p, pl, sms, st);
