@@ -600,8 +600,10 @@ constexpr int kTritSmem = kTritStages * kTritStageBytes + 1024;
 constexpr int kTritSplitCtas = 152;        // split K while fewer CTAs than this would run
 constexpr int kTritMaxSplit = 4;           // cluster size (8 measured slower)
 constexpr int kTritMinStages = 4;          // beats per split, at least
-constexpr int kPartPitch = kTileN + 4;     // partial tile [m][n] row pitch (conflict-free)
-static_assert(2 * kTileM * kPartPitch * 4 <= kTritStages * kTritStageBytes,
+// the partial tiles of one output pass, [token][column] with a 4-float pad (conflict-free):
+// 256 tokens x 128 columns, or 128 tokens x 256 columns (one token tile, or a split-K CTA)
+static_assert(2 * kTileM * (kTileN + 4) * 4 <= kTritStages * kTritStageBytes &&
+                  kTileM * (2 * kTileN + 4) * 4 <= kTritStages * kTritStageBytes,
               "the partial tiles must fit in the stage ring");
 
 struct TritGemmMat {
@@ -800,112 +802,158 @@ __global__ void __launch_bounds__(kTritThreads, 1)
         }
     }
 
-    // Output, in two passes of 128 weight rows (the shared memory holds one pass's partials).
-    // Warps 0-7 read the accumulators (warp w: lane quarter w % 4 of token tile w / 4) and park
-    // them in the idle stage ring as [token][column] tiles; then every CTA of the cluster (one CTA
-    // when K is not split) has its partials parked.  Rows are dealt to the ks CTAs in turn; a
-    // warp writes one whole 128-column row per step, lane l taking columns 4l .. 4l + 3
-    // (coalesced 512-byte stores), after adding the ks partials of that row over the cluster
-    // through distributed shared memory.  Integer partials: every sum is an integer below 2^24,
-    // exact in any order; y takes the two roundings of the planar GEMV.  The barriers are reached
-    // by every thread of every CTA the same number of times, whatever its role.
+    // Output.  Integer partials: every sum is an integer below 2^24, exact in any order; y takes
+    // the two roundings of the planar GEMV.  Rows of y are written by whole warps, lane l taking
+    // columns 4l .. 4l + 3 of every 128 (coalesced 512-byte stores).
     if (warp < kTritExpWarps) {
         if (!__all_sync(0xffffffffu, mbar_wait(&mma_done, 0)) && lane == 0) atomicOr(p.err, 1);
         tc_fence_after();
     }
-    for (int pass = 0; pass < 2; pass++) {
-        const int64_t nbase = n0 + pass * kTileN;
+    // Writes y[m0 + rr][nbase + 128 g + 4 lane ..] (and acc) from the integer sums a.
+    auto store_row = [&](int rr, int g, int64_t nbase, const float4 &a) {
+        const int64_t m = m0 + rr;
+        const int64_t nb = nbase + g * kTileN + 4 * lane;
+        const float xs = xs_tile[rr];
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        float o[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) o[j] = __fmul_rn(__fmul_rn(av[j], xs), W.w_scale);
+        float *yrow = W.y + m * (int64_t)W.N;
+        int32_t *arow = W.acc ? W.acc + m * (int64_t)W.N : nullptr;
+        if ((W.N & 3) == 0 && nb + 4 <= W.N) {
+            *reinterpret_cast<float4 *>(yrow + nb) = make_float4(o[0], o[1], o[2], o[3]);
+            if (arow)
+                *reinterpret_cast<int4 *>(arow + nb) =
+                    make_int4(__float2int_rn(av[0]), __float2int_rn(av[1]),
+                              __float2int_rn(av[2]), __float2int_rn(av[3]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                if (nb + j < W.N) {
+                    yrow[nb + j] = o[j];
+                    if (arow) arow[nb + j] = __float2int_rn(av[j]);
+                }
+            }
+        }
+    };
+    if (p.ks > 1) {
+        // K split over the cluster (one token tile per CTA): every split parks its 128 x 256
+        // partial tile in its idle stage ring ([token][column], 4-float pad: conflict-free); after
+        // a cluster barrier each CTA adds the ks partials of its share of the token rows through
+        // distributed shared memory, two rows per warp at a time with every load in flight
+        // together; a last cluster barrier keeps every CTA's partials alive until all are read.
+        constexpr int pitch = kTritTileN + 4;
         if (warp < kTritExpWarps) {
-            const int h = warp >> 2, q = warp & 3;
-            if (h < halves) {
-                const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) +
-                                    (uint32_t)(h * kTritTileN + pass * kTileN);
-                const int row = h * kTileM + q * 32 + lane;
+            const int q = warp & 3, g = warp >> 2;  // lane quarter, column half
+            const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(g * kTileN);
+            float *dst = part + (q * 32 + lane) * pitch + g * kTileN;
 #pragma unroll 1
-                for (int c = 0; c < kTileN / 32; c++) {
-                    uint32_t r[32];
-                    __syncwarp();  // the tensor-memory load is warp-collective
-                    tmem_ld32(tl + 32 * c, r);
-                    float4 *dst = reinterpret_cast<float4 *>(part + row * kPartPitch + 32 * c);
+            for (int c = 0; c < kTileN / 32; c++) {
+                uint32_t r[32];
+                __syncwarp();  // the tensor-memory load is warp-collective
+                tmem_ld32(tl + 32 * c, r);
 #pragma unroll
-                    for (int v = 0; v < 8; v++)
-                        dst[v] = make_float4(__uint_as_float(r[4 * v]),
-                                             __uint_as_float(r[4 * v + 1]),
-                                             __uint_as_float(r[4 * v + 2]),
-                                             __uint_as_float(r[4 * v + 3]));
-                }
+                for (int v = 0; v < 8; v++)
+                    *reinterpret_cast<float4 *>(dst + 32 * c + 4 * v) =
+                        make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
             }
         }
         __syncwarp();
-        if (p.ks > 1)
-            cluster_sync_all();
-        else
-            __syncthreads();
-        if (warp < kTritExpWarps && nbase < W.N) {
-            const int nrows = halves * kTileM;
-            const int64_t nb = nbase + 4 * lane;
-            const bool full4 = (W.N & 3) == 0 && nb + 4 <= W.N;
-            for (int rr = split * kTritExpWarps + warp; rr < nrows;
-                 rr += kTritExpWarps * p.ks) {
-                const int64_t m = m0 + rr;
-                if (m >= p.M) break;  // rows run upward: the rest of the tile is past M as well
-                const float *src = part + rr * kPartPitch + 4 * lane;
-                float4 a = *reinterpret_cast<const float4 *>(src);
-                if (p.ks > 1) {
-                    const uint32_t local = smem_u32(src);
-                    float4 t[kTritMaxSplit];
+        cluster_sync_all();
+        if (warp < kTritExpWarps) {
+            const int rstep = kTritExpWarps * p.ks;
+            for (int r0 = split * kTritExpWarps + warp; r0 < kTileM; r0 += 2 * rstep) {
+                if (m0 + r0 >= p.M) break;  // rows run upward: the rest is past M as well
+                float4 a[2][2];
 #pragma unroll
-                    for (int s = 0; s < kTritMaxSplit; s++) {
-                        t[s] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (s < p.ks && s != split) {
-                            uint32_t remote;
+                for (int u = 0; u < 2; u++) {
+                    const int rr = r0 + u * rstep;
+                    const bool live = rr < kTileM && m0 + rr < p.M;
+#pragma unroll
+                    for (int g = 0; g < 2; g++) {
+                        a[u][g] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (!live) continue;
+                        const uint32_t local = smem_u32(part + rr * pitch + g * kTileN + 4 * lane);
+#pragma unroll
+                        for (int sp = 0; sp < kTritMaxSplit; sp++) {
+                            if (sp >= p.ks) break;
+                            uint32_t addr;
+                            float4 t;
                             asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                                         : "=r"(remote) : "r"(local), "r"((uint32_t)s));
+                                         : "=r"(addr) : "r"(local), "r"((uint32_t)sp));
                             asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                         : "=f"(t[s].x), "=f"(t[s].y), "=f"(t[s].z),
-                                           "=f"(t[s].w)
-                                         : "r"(remote));
+                                         : "=f"(t.x), "=f"(t.y), "=f"(t.z), "=f"(t.w)
+                                         : "r"(addr));
+                            a[u][g].x += t.x;
+                            a[u][g].y += t.y;
+                            a[u][g].z += t.z;
+                            a[u][g].w += t.w;
                         }
-                    }
-#pragma unroll
-                    for (int s = 0; s < kTritMaxSplit; s++) {
-                        a.x += t[s].x;
-                        a.y += t[s].y;
-                        a.z += t[s].z;
-                        a.w += t[s].w;
                     }
                 }
-                const float xs = xs_tile[rr];
-                const float av[4] = {a.x, a.y, a.z, a.w};
-                float o[4];
 #pragma unroll
-                for (int j = 0; j < 4; j++) o[j] = __fmul_rn(__fmul_rn(av[j], xs), W.w_scale);
-                float *yrow = W.y + m * (int64_t)W.N;
-                int32_t *arow = W.acc ? W.acc + m * (int64_t)W.N : nullptr;
-                if (full4) {
-                    *reinterpret_cast<float4 *>(yrow + nb) = make_float4(o[0], o[1], o[2], o[3]);
-                    if (arow)
-                        *reinterpret_cast<int4 *>(arow + nb) =
-                            make_int4(__float2int_rn(av[0]), __float2int_rn(av[1]),
-                                      __float2int_rn(av[2]), __float2int_rn(av[3]));
-                } else {
+                for (int u = 0; u < 2; u++) {
+                    const int rr = r0 + u * rstep;
+                    if (rr >= kTileM || m0 + rr >= p.M) break;
 #pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        if (nb + j < W.N) {
-                            yrow[nb + j] = o[j];
-                            if (arow) arow[nb + j] = __float2int_rn(av[j]);
-                        }
-                    }
+                    for (int g = 0; g < 2; g++) store_row(rr, g, n0, a[u][g]);
                 }
             }
         }
-        // every partial read before the next pass overwrites it (and, split, before any CTA of
-        // the cluster exits)
         __syncwarp();
-        if (p.ks > 1)
-            cluster_sync_all();
-        else
+        cluster_sync_all();
+    } else {
+        // One CTA per tile: the partials are parked in the idle stage ring as [token][column]
+        // tiles -- all 256 weight rows at once for one token tile (128 x 256 fits), in two passes
+        // of 128 rows for two -- by warps 0-7 (lane quarter w % 4; token tile, or with one token
+        // tile column half, w / 4), then written row by row.
+        const int npass = halves == 1 ? 1 : 2;
+        const int ngrp = halves == 1 ? 2 : 1;    // 128-column groups per pass
+        const int pitch = ngrp * kTileN + 4;      // partial row pitch in floats (conflict-free)
+        for (int pass = 0; pass < npass; pass++) {
+            const int64_t nbase = n0 + pass * kTileN;
+            if (warp < kTritExpWarps) {
+                const int hi = warp >> 2, q = warp & 3;
+                const int h = halves == 1 ? 0 : hi;  // token tile
+                const int g = halves == 1 ? hi : 0;  // column group within the pass
+                if (h < halves) {
+                    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) +
+                                        (uint32_t)(h * kTritTileN + pass * kTileN + g * kTileN);
+                    const int row = h * kTileM + q * 32 + lane;
+#pragma unroll 1
+                    for (int c = 0; c < kTileN / 32; c++) {
+                        uint32_t r[32];
+                        __syncwarp();  // the tensor-memory load is warp-collective
+                        tmem_ld32(tl + 32 * c, r);
+                        float4 *dst =
+                            reinterpret_cast<float4 *>(part + row * pitch + g * kTileN + 32 * c);
+#pragma unroll
+                        for (int v = 0; v < 8; v++)
+                            dst[v] = make_float4(__uint_as_float(r[4 * v]),
+                                                 __uint_as_float(r[4 * v + 1]),
+                                                 __uint_as_float(r[4 * v + 2]),
+                                                 __uint_as_float(r[4 * v + 3]));
+                    }
+                }
+            }
             __syncthreads();
+            if (warp < kTritExpWarps && nbase < W.N) {
+                const int nrows = halves * kTileM;
+                for (int rr = warp; rr < nrows; rr += kTritExpWarps) {
+                    if (m0 + rr >= p.M) break;  // rows run upward: the rest is past M as well
+#pragma unroll
+                    for (int g = 0; g < 2; g++) {
+                        if (g >= ngrp) break;
+                        store_row(rr, g, nbase,
+                                  *reinterpret_cast<const float4 *>(part + rr * pitch +
+                                                                    g * kTileN + 4 * lane));
+                    }
+                }
+            }
+            // every partial read before the next pass overwrites it
+            __syncthreads();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -951,8 +999,10 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
     const int nst = (int)(K / 64);
     // Split K when the tiles alone would leave SMs idle (ks * tiles <= kTritSplitCtas), with at
     // least kTritMinStages beats per split and no split empty.
+    // Only one-token-tile CTAs split (a 128 x 256 partial tile fits the idle stage ring).
     int ks = (int)std::min<int64_t>(kTritMaxSplit, std::max<int64_t>(1, kTritSplitCtas / tiles));
     ks = std::min(ks, std::max(1, nst / kTritMinStages));
+    if (mstep != 1) ks = 1;
     const int sps = (nst + ks - 1) / ks;
     ks = (nst + sps - 1) / sps;
     DeviceInfo di;
