@@ -131,6 +131,22 @@ __device__ __forceinline__ void tmem_ld32_pairs(uint32_t taddr, uint64_t (&p)[16
         : "memory");
 }
 
+// Half of that load: 16 consecutive columns as 8 pairs.
+__device__ __forceinline__ void tmem_ld16_pairs(uint32_t taddr, uint64_t (&p)[8]) {
+    asm volatile(
+        "{ .reg .b32 r<16>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {r0,r1,r2,r3,r4,r5,r6,r7,r8,r9,r10,r11,r12,r13,"
+        "r14,r15}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {r0, r1}; mov.b64 %1, {r2, r3}; mov.b64 %2, {r4, r5};\n\t"
+        "mov.b64 %3, {r6, r7}; mov.b64 %4, {r8, r9}; mov.b64 %5, {r10, r11};\n\t"
+        "mov.b64 %6, {r12, r13}; mov.b64 %7, {r14, r15}; }"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]),
+          "=l"(p[7])
+        : "r"(taddr)
+        : "memory");
+}
+
 // acc += a * {s, s} on pairs of binary32 (element 0 in the low half), each element rounded once
 // as by fmaf.
 __device__ __forceinline__ void ffma2p(uint64_t &acc, uint64_t a, uint64_t s2) {

@@ -454,21 +454,33 @@ __global__ void __launch_bounds__(kTgThreads, 1)
                         } else {
                             // token pairs (2k, 2k + 1): column pair 8t + k holds their S_hi, pair
                             // 8t + 4 + k their S_lo; two tokens per f32x2 instruction
-                            uint64_t pr[16];
-                            tmem_ld32_pairs(taddr, pr);
-                            if (pb == kTgBlocks / 2 - 1) {
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(&t_empty[tb]);
-                            }
+                            // 7-8 tokens: one block's 16 columns per load (the 32-column
+                            // load left too few registers there); 5-6 tokens: both blocks at once
+                            constexpr bool kHalf = B >= 7;
+                            uint64_t pw[kHalf ? 8 : 16];
+                            if (!kHalf) tmem_ld32_pairs(taddr, reinterpret_cast<uint64_t (&)[16]>(pw));
 #pragma unroll
                             for (int t = 0; t < 2; t++) {
+                                uint64_t pr[8];
+                                if (kHalf) {
+                                    tmem_ld16_pairs(taddr + 16 * t, reinterpret_cast<uint64_t (&)[8]>(pw));
+#pragma unroll
+                                    for (int i = 0; i < 8; i++) pr[i] = pw[i];
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 8; i++) pr[i] = pw[8 * t + i];
+                                }
+                                if (pb == kTgBlocks / 2 - 1 && (kHalf ? t == 1 : t == 0)) {
+                                    tc_fence_before();
+                                    __syncwarp();
+                                    if (lane == 0) mbar_arrive(&t_empty[tb]);
+                                }
                                 const int jb = 2 * pb + t;
                                 const uint64_t *dxq = reinterpret_cast<const uint64_t *>(dxf + (j0 + jb) * 8);
 #pragma unroll
                                 for (int k = 0; k < NP; k++) {
-                                    uint64_t is2 = pr[8 * t + 4 + k];
-                                    ffma2p(is2, pr[8 * t + k], kSixteen2);  // 16 S_hi + S_lo, exact
+                                    uint64_t is2 = pr[4 + k];
+                                    ffma2p(is2, pr[k], kSixteen2);  // 16 S_hi + S_lo, exact
                                     if (F == kTrit)
                                         ffma2p(acc2[k], is2, kOne2);        // acc += isum, exact
                                     else
