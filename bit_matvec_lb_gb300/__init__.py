@@ -21,7 +21,8 @@ __all__ = [
     "lb_gemv_q1_0_grouped", "lb_gemv_q2_0_g64_grouped", "lb_gemv_trit_planes_grouped",
     "lb_gemm_workspace_bytes", "lb_gemm_q1_0", "lb_gemm_q2_0_g64", "lb_gemm_q1_0_grouped",
     "lb_gemm_q2_0_g64_grouped", "lb_gemm_q2_0_g64_noalloc", "lb_gemm_trit_workspace_bytes",
-    "lb_gemm_trit_planes", "lb_gemm_trit_planes_grouped", "lb_dequantize_q1_0",
+    "lb_gemm_trit_planes", "lb_gemm_trit_planes_grouped", "lb_quantize_i8_absmax_tiles",
+    "lb_gemm_trit_planes_grouped_tiles", "lb_dequantize_q1_0",
     "lb_dequantize_q2_0_g64", "lb_dequantize_trit_planes", "OUT_F32", "OUT_BF16",
     "lb_pack_base3", "lb_gemv_base3", "base3_row_bytes", "lb_test_inject_wait_timeout",
 ]
@@ -95,6 +96,9 @@ SIGNATURES = {
     "lb_gemm_trit_planes": (I32, [P, F32, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, P]),
     "lb_gemm_trit_planes_grouped": (I32, [ctypes.POINTER(lb_trit_matrix), I32, P, P, I64, I64, P,
                                           ctypes.c_size_t, P]),
+    "lb_quantize_i8_absmax_tiles": (I32, [P, P, P, I64, I64, P, ctypes.c_size_t, P]),
+    "lb_gemm_trit_planes_grouped_tiles": (I32, [ctypes.POINTER(lb_trit_matrix), I32, P, I64, I64,
+                                                P, ctypes.c_size_t, P]),
     "lb_dequantize_q1_0": (I32, [P, P, I64, I64, I32, P, P]),
     "lb_dequantize_q2_0_g64": (I32, [P, P, I64, I64, I32, P, P]),
     "lb_dequantize_trit_planes": (I32, [P, F32, I64, I64, I32, P, P]),
@@ -358,6 +362,32 @@ def lb_gemm_trit_planes_grouped(mats, q, x_scale, M: int, K: int, workspace,
     _check("lb_gemm_trit_planes_grouped", load().lb_gemm_trit_planes_grouped(
         arr, len(mats), _ptr(q), _ptr(x_scale), int(M), int(K), _ptr(workspace),
         int(workspace_bytes), _stream(stream)))
+
+
+def lb_quantize_i8_absmax_tiles(x, q, x_scale, M: int, K: int, workspace, workspace_bytes=None,
+                                stream=None):
+    """lb_quantize_i8_absmax that also writes the planar GEMM's activation operand tiles into
+    workspace (for lb_gemm_trit_planes_grouped_tiles)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("lb_quantize_i8_absmax_tiles", load().lb_quantize_i8_absmax_tiles(
+        _ptr(x), _ptr(q), _ptr(x_scale), int(M), int(K), _ptr(workspace), int(workspace_bytes),
+        _stream(stream)))
+
+
+def lb_gemm_trit_planes_grouped_tiles(mats, x_scale, M: int, K: int, workspace,
+                                      workspace_bytes=None, stream=None):
+    """lb_gemm_trit_planes_grouped from the operand tiles lb_quantize_i8_absmax_tiles wrote."""
+    if not 1 <= len(mats) <= GEMM_MAX_GROUP:
+        raise ValueError(f"a GEMM group holds 1..{GEMM_MAX_GROUP} matrices")
+    arr = (lb_trit_matrix * len(mats))()
+    for i, (planes, w_scale, y, acc, N) in enumerate(mats):
+        arr[i] = lb_trit_matrix(_ptr(planes), float(w_scale), _ptr(y), _ptr(acc), int(N))
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("lb_gemm_trit_planes_grouped_tiles", load().lb_gemm_trit_planes_grouped_tiles(
+        arr, len(mats), _ptr(x_scale), int(M), int(K), _ptr(workspace), int(workspace_bytes),
+        _stream(stream)))
 
 
 def lb_dequantize_q1_0(bits, scales, N: int, K: int, out_format: int, out, stream=None):

@@ -125,6 +125,20 @@ __device__ __forceinline__ uint32_t nor_u32(uint32_t a, uint32_t b) {
     return d;
 }
 
+// Per-token int8 quantization of four values: rne(v * s) clamped to [-128, 127], packed
+// little-endian (shared by lb_quantize_i8_absmax and its operand-writing variant).
+__device__ __forceinline__ uint32_t quantize_i8_word(float4 v, float s) {
+    const int c[4] = {__float2int_rn(__fmul_rn(v.x, s)), __float2int_rn(__fmul_rn(v.y, s)),
+                      __float2int_rn(__fmul_rn(v.z, s)), __float2int_rn(__fmul_rn(v.w, s))};
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int t = c[j] > 127 ? 127 : (c[j] < -128 ? -128 : c[j]);
+        w |= (uint32_t)(t & 0xFF) << (8 * j);
+    }
+    return w;
+}
+
 __device__ __forceinline__ float f16_bits_to_float(uint16_t h) {
     return __half2float(__ushort_as_half(h));
 }

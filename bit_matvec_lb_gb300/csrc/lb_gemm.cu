@@ -88,7 +88,6 @@ __global__ void __launch_bounds__(256) gemm_prep_act_kernel(const int8_t *__rest
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += stride)
         zero[i] = 0;
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
         const int r = (int)(i % kTileM);
         const int64_t tj = i / kTileM;
@@ -110,18 +109,7 @@ __global__ void __launch_bounds__(256) gemm_prep_act_kernel(const int8_t *__rest
         for (int kc = 0; kc < 4; kc++) {
             const uint32_t x = F == kG2 ? a[4 * (kc >> 1) + (kc & 1)] : a[kc];
             const uint32_t y = F == kG2 ? a[4 * (kc >> 1) + (kc & 1) + 2] : a[kc + 4];
-            const uint32_t lo = prmt(x, y, 0x5140) ^ 0x80808080u;  // x0 y0 x1 y1, biased +128
-            const uint32_t hi = prmt(x, y, 0x7362) ^ 0x80808080u;  // x2 y2 x3 y3
-            // f16 with exponent byte 0x64: 1024 + (q + 128); subtracting 1152 (0x6480) gives q
-            uint32_t h[4] = {prmt(lo, 0x64646464u, 0x5140), prmt(lo, 0x64646464u, 0x7362),
-                             prmt(hi, 0x64646464u, 0x5140), prmt(hi, 0x64646464u, 0x7362)};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&h[e]), bias);
-                h[e] = *reinterpret_cast<uint32_t *>(&v);
-            }
-            *reinterpret_cast<uint4 *>(tile + canon_offset(r, kc * 8)) =
-                make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(tile + canon_offset(r, kc * 8)) = int8_pair_f16(x, y);
         }
     }
 }
@@ -963,12 +951,93 @@ __global__ void __launch_bounds__(kTritThreads, 1)
     }
 }
 
+// Per-token absmax int8 quantization (lb_quantize_i8_absmax: s = 127 / amax, q = rne(x s)
+// clamped, x_scale = amax / 127) that also writes the planar GEMM's activation operand tiles
+// (the workspace contents its prologue would build from q).  One CTA per token row of the
+// 128-row tiles; rows past M write zero operand rows.  Thread t quantizes words t, t + 512, ...
+// (4 codes each); a 32-wide block is eight words held by eight consecutive lanes, and the lane
+// of word kc < 4 takes word kc + 4 from four lanes up to write chunk kc of the block.
+constexpr int kQTHold = 4;
+__global__ void __launch_bounds__(512) quantize_i8_tiles_kernel(const float *__restrict__ x,
+                                                               int8_t *__restrict__ q,
+                                                               float *__restrict__ x_scale,
+                                                               uint8_t *__restrict__ ws, int M,
+                                                               int K) {
+    __shared__ float red[32];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int m = blockIdx.x, lane = threadIdx.x & 31;
+    const int nK32 = K / 32, r = m % kTileM;
+    const int nq = K / 4;
+    uint8_t *tiles = ws + (int64_t)(m / kTileM) * nK32 * kTileBytes;
+    auto put = [&](int w, uint32_t a, uint32_t b) {  // word w = a, word w + 4 = b
+        if ((w & 7) < 4)
+            *reinterpret_cast<uint4 *>(tiles + (int64_t)(w >> 3) * kTileBytes +
+                                       canon_offset(r, (w & 7) * 8)) = int8_pair_f16(a, b);
+    };
+    if (m >= M) {
+        for (int w = threadIdx.x; w < nq; w += blockDim.x) put(w, 0u, 0u);
+        return;
+    }
+    const float4 *xb = reinterpret_cast<const float4 *>(x + (int64_t)m * K);
+    float a = 0.0f;
+    float4 held[kQTHold];
+#pragma unroll
+    for (int h = 0; h < kQTHold; h++) {
+        const int i = threadIdx.x + h * blockDim.x;
+        held[h] = i < nq ? xb[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 v = held[h];
+        a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    for (int i = threadIdx.x + kQTHold * blockDim.x; i < nq; i += blockDim.x) {
+        const float4 v = xb[i];
+        a = fmaxf(a, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) red[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        a = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0f;
+        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (threadIdx.x == 0) red[0] = a;
+    }
+    __syncthreads();
+    const float amax = red[0];
+    const float s = (amax != 0.0f) ? __fdiv_rn(127.0f, amax) : 0.0f;
+    if (threadIdx.x == 0) x_scale[m] = __fdiv_rn(amax, 127.0f);
+    uint32_t *qb = reinterpret_cast<uint32_t *>(q + (int64_t)m * K);
+    // every lane of a warp takes part in each shuffle (nq is a multiple of 16: a warp's words
+    // past nq are whole 8-word blocks, their results unused)
+#pragma unroll
+    for (int h = 0; h < kQTHold; h++) {
+        const int i = threadIdx.x + h * blockDim.x;
+        if (i - lane >= nq) break;
+        const uint32_t w = quantize_i8_word(held[h], s);
+        const uint32_t w4 = __shfl_down_sync(0xffffffffu, w, 4);
+        if (i < nq) {
+            qb[i] = w;
+            put(i, w, w4);
+        }
+    }
+    for (int i = threadIdx.x + kQTHold * blockDim.x; i - lane < nq; i += blockDim.x) {
+        const uint32_t w = i < nq ? quantize_i8_word(xb[i], s) : 0u;
+        const uint32_t w4 = __shfl_down_sync(0xffffffffu, w, 4);
+        if (i < nq) {
+            qb[i] = w;
+            put(i, w, w4);
+        }
+    }
+}
+
+// Checks and launches of a planar call over G matrices sharing one activation.  `q` is the
+// int8 activation (its operand tiles are built by the prologue kernel), or NULL when the
+// workspace already holds them (written by lb_quantize_i8_absmax_tiles).
 static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
                            const float *x_scale, int64_t M, int64_t K, void *workspace,
-                           size_t workspace_bytes, void *stream) {
-    if (!mats || !q || !x_scale || !workspace) return LB_ERR_NULL;
+                           size_t workspace_bytes, void *stream, bool pretiled = false) {
+    if (!mats || (!q && !pretiled) || !x_scale || !workspace) return LB_ERR_NULL;
     if (G < 1 || G > LB_GEMM_MAX_GROUP) return LB_ERR_SHAPE;
-    if (!aligned16(q) || !aligned16(x_scale) || !aligned16(workspace)) return LB_ERR_ALIGN;
+    if ((q && !aligned16(q)) || !aligned16(x_scale) || !aligned16(workspace)) return LB_ERR_ALIGN;
     if (M < 1 || M > (1 << 30) || K < 64 || K % 64 != 0 || K > (1 << 24) / 128)
         return LB_ERR_SHAPE;
     if (workspace_bytes < lb_gemm_workspace_bytes(M, K)) return LB_ERR_SHAPE;
@@ -1017,9 +1086,11 @@ static int gemm_trit_group(const lb_trit_matrix *mats, int G, const int8_t *q,
     const int64_t work = mtiles * kTileM * (K / 32);
     int64_t pgrid = (work + 255) / 256;
     if (pgrid > (int64_t)di.sms * 16) pgrid = (int64_t)di.sms * 16;
-    if (int e = launch_pdl(gemm_prep_act_kernel<kG1>, dim3((unsigned)pgrid), dim3(256), 0, st, q,
-                           (uint8_t *)workspace, (int)M, (int)K, (int)mtiles, (int *)nullptr, 0))
-        return e;
+    if (!pretiled)
+        if (int e = launch_pdl(gemm_prep_act_kernel<kG1>, dim3((unsigned)pgrid), dim3(256), 0, st,
+                               q, (uint8_t *)workspace, (int)M, (int)K, (int)mtiles,
+                               (int *)nullptr, 0))
+            return e;
     p.ws = static_cast<const uint8_t *>(workspace);
     p.x_scale = x_scale;
     p.G = G;
@@ -1062,6 +1133,30 @@ LB_EXPORT int lb_gemm_trit_planes_grouped(const lb_trit_matrix *mats, int G, con
                                           void *workspace, size_t workspace_bytes,
                                           void *stream) {
     return gemm_trit_group(mats, G, q, x_scale, M, K, workspace, workspace_bytes, stream);
+}
+
+LB_EXPORT int lb_quantize_i8_absmax_tiles(const float *x, int8_t *q, float *x_scale, int64_t M,
+                                          int64_t K, void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+    if (!x || !q || !x_scale || !workspace) return LB_ERR_NULL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(x_scale) || !aligned16(workspace))
+        return LB_ERR_ALIGN;
+    if (M < 1 || M > (1 << 30) || K < 64 || K % 64 != 0 || K > (1 << 24) / 128)
+        return LB_ERR_SHAPE;
+    if (workspace_bytes < lb_gemm_workspace_bytes(M, K)) return LB_ERR_SHAPE;
+    DeviceInfo di;
+    if (int st = current_device_info(&di)) return st;
+    const int64_t rows = (M + kTileM - 1) / kTileM * kTileM;
+    return launch_pdl(quantize_i8_tiles_kernel, dim3((unsigned)rows), dim3(512), 0,
+                      as_stream(stream), x, q, x_scale, (uint8_t *)workspace, (int)M, (int)K);
+}
+
+LB_EXPORT int lb_gemm_trit_planes_grouped_tiles(const lb_trit_matrix *mats, int G,
+                                                const float *x_scale, int64_t M, int64_t K,
+                                                void *workspace, size_t workspace_bytes,
+                                                void *stream) {
+    return gemm_trit_group(mats, G, nullptr, x_scale, M, K, workspace, workspace_bytes, stream,
+                           true);
 }
 
 LB_EXPORT int lb_gemm_trit_planes(const uint64_t *planes, float w_scale, const int8_t *q,

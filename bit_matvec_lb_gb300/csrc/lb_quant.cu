@@ -48,18 +48,6 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__rest
 // K = 512 * 4 * kHold); the rest of a longer row is read twice.
 constexpr int kHold = 4;
 
-__device__ __forceinline__ uint32_t quantize_i8_word(float4 v, float s) {
-    const int c[4] = {__float2int_rn(__fmul_rn(v.x, s)), __float2int_rn(__fmul_rn(v.y, s)),
-                      __float2int_rn(__fmul_rn(v.z, s)), __float2int_rn(__fmul_rn(v.w, s))};
-    uint32_t w = 0;
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const int t = c[j] > 127 ? 127 : (c[j] < -128 ? -128 : c[j]);
-        w |= (uint32_t)(t & 0xFF) << (8 * j);
-    }
-    return w;
-}
-
 __global__ void __launch_bounds__(512) quantize_i8_absmax_kernel(const float *__restrict__ x,
                                                                  int8_t *__restrict__ q,
                                                                  float *__restrict__ x_scale,

@@ -19,6 +19,23 @@ __device__ __forceinline__ int canon_offset(int r, int k) {
     return (r >> 3) * kCoreSBO + (k >> 3) * kCoreLBO + (r & 7) * 16 + (k & 7) * 2;
 }
 
+// Eight f16 of K for one row of an activation operand tile from two words of int8 codes x, y:
+// x0 y0 x1 y1 x2 y2 x3 y3 (f16x2 number i pairs byte i of x with byte i of y).  Exact: each code
+// is biased by +128 into the mantissa of 1024 (exponent byte 0x64) and 1152 is subtracted.
+__device__ __forceinline__ uint4 int8_pair_f16(uint32_t x, uint32_t y) {
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const uint32_t lo = prmt(x, y, 0x5140) ^ 0x80808080u;  // x0 y0 x1 y1, biased +128
+    const uint32_t hi = prmt(x, y, 0x7362) ^ 0x80808080u;  // x2 y2 x3 y3
+    uint32_t h[4] = {prmt(lo, 0x64646464u, 0x5140), prmt(lo, 0x64646464u, 0x7362),
+                     prmt(hi, 0x64646464u, 0x5140), prmt(hi, 0x64646464u, 0x7362)};
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        __half2 v = __hsub2(*reinterpret_cast<__half2 *>(&h[e]), bias);
+        h[e] = *reinterpret_cast<uint32_t *>(&v);
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
 // Shared-memory matrix descriptor: start address, LBO, SBO (all >> 4), version 1, no swizzle.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
     uint64_t d = 0;

@@ -294,6 +294,23 @@ int lb_gemm_trit_planes_grouped(const lb_trit_matrix *mats, int G, const int8_t 
                                 const float *x_scale, int64_t M, int64_t K, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
+/* Quantize-then-GEMM in two launches instead of three: lb_quantize_i8_absmax_tiles quantizes x
+ * [M][K] fp32 exactly as lb_quantize_i8_absmax (q and x_scale bit-identical) and also writes into
+ * `workspace` the activation operand tiles that lb_gemm_trit_planes* would build from q in a
+ * prologue launch; lb_gemm_trit_planes_grouped_tiles then runs the grouped planar GEMM from those
+ * tiles (no q argument, no prologue).  Outputs, limits and errors as lb_gemm_trit_planes_grouped.
+ *   workspace : at least lb_gemm_trit_workspace_bytes(M, K) bytes; between the two calls it must
+ *               not be used by any other call (the GEMM reads the tiles the quantizer wrote;
+ *               several GEMMs may read them in turn, for example q|k|v and a second group).
+ * Limits of the quantizer: 1 <= M <= 2^30; K % 64 == 0, 64 <= K <= 2^24 / 128.  Errors:
+ * LB_ERR_NULL, LB_ERR_ALIGN (x, q, x_scale or workspace not 16-byte aligned), LB_ERR_SHAPE
+ * (limits, or a workspace too small), LB_ERR_ARCH, LB_ERR_LAUNCH. */
+int lb_quantize_i8_absmax_tiles(const float *x, int8_t *q, float *x_scale, int64_t M, int64_t K,
+                                void *workspace, size_t workspace_bytes, void *stream);
+int lb_gemm_trit_planes_grouped_tiles(const lb_trit_matrix *mats, int G, const float *x_scale,
+                                      int64_t M, int64_t K, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
 /* ---------------------------------------------------------------------------------------
  * Dequantization ([TR] III.4 and IV.2: every weight of a tensor dequantized and compared with
  * the reference's floats; III.2 and III.5 define w).  Every weight as the binary32 product

@@ -242,6 +242,36 @@ def test_gemm_trit_refusals(lib):
     assert g(arr, 2, A, A, 16, K, A, ws, None) == -3      # N = 0
 
 
+def test_quantize_tiles_and_pretiled_gemm_refusals(lib):
+    """The quantize-then-GEMM pair refuses on the host before anything is enqueued."""
+    f = lib.lb_quantize_i8_absmax_tiles
+    K = 256
+    ws = lib.lb_gemm_trit_workspace_bytes(16, K)
+    ok = [A, A, A, 16, K, A, ws, None]
+    for i in (0, 1, 2, 5):
+        args = list(ok)
+        args[i] = None
+        assert f(*args) == -1
+        args[i] = MIS
+        assert f(*args) == -2
+    for M, KK in ((0, K), (2**31, K), (16, 32), (16, K + 16), (16, 0),
+                  (16, (1 << 24) // 128 + 64)):
+        assert f(A, A, A, M, KK, A, 2**40, None) == -3
+    assert f(A, A, A, 16, K, A, ws - 1, None) == -3       # workspace short
+    g = lib.lb_gemm_trit_planes_grouped_tiles
+    arr = (lb.lb_trit_matrix * 9)()
+    for i in range(9):
+        arr[i] = lb.lb_trit_matrix(A, 1.0, A, None, 8)
+    assert g(None, 1, A, 16, K, A, ws, None) == -1        # no matrices
+    assert g(arr, 1, None, 16, K, A, ws, None) == -1      # no x_scale
+    assert g(arr, 1, A, 16, K, None, ws, None) == -1      # no workspace
+    assert g(arr, 1, MIS, 16, K, A, ws, None) == -2
+    assert g(arr, 0, A, 16, K, A, ws, None) == -3         # empty group
+    assert g(arr, 9, A, 16, K, A, ws, None) == -3         # more than LB_GEMM_MAX_GROUP
+    assert g(arr, 1, A, 16, K + 32, A, 2**40, None) == -3  # K % 64
+    assert g(arr, 1, A, 16, K, A, ws - 1, None) == -3     # workspace short
+
+
 # ---- dequantization: host checks ----
 @pytest.mark.parametrize("fn,qk", [("lb_dequantize_q1_0", 128), ("lb_dequantize_q2_0_g64", 64)])
 def test_dequant_refusals(lib, fn, qk):

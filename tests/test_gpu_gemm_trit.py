@@ -160,3 +160,43 @@ def test_gemm_trit_prefill_shapes_sampled(name, N, K):
 
 def test_gemm_trit_device_status_clean():
     assert lb.lb_device_status() == 0
+
+
+@pytest.mark.parametrize("M,K,Ns", [(1, 64, (3,)), (130, 1216, (130, 1, 257)),
+                                    (300, 2560, (640, 2560)), (512, 6912, (2560,))])
+def test_quantize_tiles_then_gemm(M, K, Ns):
+    """lb_quantize_i8_absmax_tiles writes q and x_scale bit-identical to lb_quantize_i8_absmax
+    (and to the oracle's quantizer) plus the GEMM's operand tiles, from which
+    lb_gemm_trit_planes_grouped_tiles gives acc and y bit-identical to the oracle; rows of the
+    last 128-token tile past M are written too (as zeros) and a second group reads the same
+    tiles."""
+    x = synth.activations(M, K, seed=40 + M)
+    q_ref, xs_ref = oracle.quantize_i8_absmax(x)
+    xd = dev(x)
+    q = guarded((M, K), torch.int8)
+    xs = guarded((M,), torch.float32, float("nan"))
+    ws = guarded(lb.lb_gemm_trit_workspace_bytes(M, K), torch.uint8, 0xFF)
+    lb.lb_quantize_i8_absmax_tiles(xd, q, xs, M, K, ws)
+    q2 = guarded((M, K), torch.int8)
+    xs2 = guarded((M,), torch.float32, float("nan"))
+    lb.lb_quantize_i8_absmax(xd, q2, xs2, M, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(q), q_ref) and np.array_equal(host(q2), q_ref)
+    assert np.array_equal(host(xs).view(np.uint32), np.asarray(xs_ref, np.float32).view(np.uint32))
+    assert np.array_equal(host(xs).view(np.uint32), host(xs2).view(np.uint32))
+    for rep in range(2):
+        mats, outs = [], []
+        for i, n in enumerate(Ns):
+            planes, _ = synth.trit_planes(n, K, seed=80 + 7 * i + rep)
+            w = synth.w_scale(90 + i + rep)
+            y = guarded((M, n), torch.float32, float("nan"))
+            acc = guarded((M, n), torch.int32)
+            mats.append((dev(planes), w, y, acc, n))
+            outs.append((planes, w, y, acc))
+        lb.lb_gemm_trit_planes_grouped_tiles(mats, xs, M, K, ws)
+        torch.cuda.synchronize()
+        for planes, w, y, acc in outs:
+            acc_ref, y_ref = oracle.trit_planes_product(planes, w, q_ref, xs_ref)
+            assert np.array_equal(host(acc), acc_ref)
+            assert np.array_equal(host(y).view(np.uint32), y_ref.view(np.uint32))
+    assert lb.lb_device_status() == 0
