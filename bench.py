@@ -456,6 +456,7 @@ def rows_measure(lb, out, which: str = "all"):
         rows_base3(lb, rows, stream)
     if which in ("all", "prefill"):
         rows_prefill(lb, rows, stream)
+        rows_tensor_rates(rows)
     out["rows"] = rows
 
 
@@ -701,6 +702,32 @@ def rows_base3(lb, rows, stream):
     rows["base3_vs_planar_16384x8192"] = out
     del planes, packed
     torch.cuda.empty_cache()
+
+
+def rows_tensor_rates(rows):
+    """Dense instruction rates of the tensor-core forms an exact prefill GEMM could use, measured
+    on this GPU by the probe library (one CTA per SM, operands resident, back-to-back MMAs)."""
+    import ctypes
+    from bit_matvec_lb_gb300 import build as lbbuild
+    try:
+        probe = ctypes.CDLL(lbbuild.PROBE_LIB)
+    except OSError as e:
+        rows["tensor_rates_probe"] = {"unavailable": str(e)}
+        return
+    probe.lbp_tensor_rates.restype = ctypes.c_int
+    probe.lbp_tensor_rates.argtypes = [ctypes.POINTER(ctypes.c_double)]
+    r = (ctypes.c_double * 4)()
+    st = probe.lbp_tensor_rates(r)
+    tflops, _ = peaks(tensor=True)
+    names = ["tcgen05_f16_m128n256k16", "tcgen05_f8f6f4_e4m3_m128n256k32",
+             "mma_sync_f16_m16n8k16", "mma_sync_s8_m16n8k32"]
+    rows["tensor_rates_probe"] = {
+        "status": st,
+        **{n: {"TFLOP/s": round(v / 1e12, 1), "frac_of_bf16_peak": round(v / 1e12 / tflops, 3)}
+           for n, v in zip(names, r)},
+        "note": "dense 2MNK per MMA, one CTA per SM, zero operands resident; the exact GEMMs run "
+                "kind::f16 (the integer kinds are not available), so its rate and the measured "
+                "cuBLAS bf16 figure are the prefill denominators"}
 
 
 def rows_prefill(lb, rows, stream):

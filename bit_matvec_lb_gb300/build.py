@@ -4,6 +4,8 @@
 
 Each .cu under csrc/ is compiled in parallel to an object, then linked with the static CUDA
 runtime into bit_matvec_lb_gb300/_build/liblb.so.  Only the lb_* entry points are exported.
+The instruction-rate probes under probe/ (a measurement library the bench loads, not part of
+the C ABI) are linked the same way into _build/liblbprobe.so.
 """
 from __future__ import annotations
 
@@ -20,6 +22,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblb.so")
+PROBE = os.path.join(HERE, "probe")
+PROBE_LIB = os.path.join(BUILD, "liblbprobe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC",
@@ -42,11 +46,18 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(INCLUDE, "lb.h")]
 
 
+def _probe_sources():
+    return sorted(glob.glob(os.path.join(PROBE, "*.cu")))
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
-        return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _deps())
+    for lib, deps in ((LIB, _deps()), (PROBE_LIB, _deps() + _probe_sources())):
+        if not os.path.exists(lib):
+            return False
+        t = os.path.getmtime(lib)
+        if not all(os.path.getmtime(p) <= t for p in deps):
+            return False
+    return True
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
@@ -55,7 +66,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
-    srcs = _sources()
+    psrcs = _probe_sources()
+    srcs = _sources() + psrcs
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def compile_one(src, obj):
@@ -69,12 +81,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         list(ex.map(lambda p: compile_one(*p), zip(srcs, objs)))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    nprobe = len(psrcs)
+    for lib, lobjs in ((LIB, objs[:len(objs) - nprobe]), (PROBE_LIB, objs[len(objs) - nprobe:])):
+        if not lobjs:
+            continue
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *lobjs, "-cudart", "static"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 
