@@ -95,3 +95,17 @@ def test_unit_scales_tensor_core_kernel(qk, B, K):
     y = _run_group(qk, Ns, blocks, q, dx)
     assert np.array_equal(y.astype(np.int64), want)
     assert lb.lb_device_status() == 0
+
+
+def test_unit_scales_streaming_q1_eight_rows_per_warp():
+    """A one-token Q1_0 call with enough 64-row tiles (601 of them, against 1201 of 32 rows, for
+    304 CTA slots: 2 waves x 7/4 < 4 waves) takes the eight-rows-per-warp streaming kernel; with
+    unit scales its outputs equal the integer block sums bit for bit, ragged last tile included."""
+    K = 256
+    Ns = [3840] * 9 + [3841]
+    blocks = _unit_blocks(128, sum(Ns), K, seed=7600)
+    q = synth.int8_codes(1, K, seed=7601)
+    want, dx = _expect(128, blocks, q)
+    y = _run_group(128, Ns, blocks, q, dx)
+    assert np.array_equal(y.astype(np.int64), want)
+    assert lb.lb_device_status() == 0
