@@ -580,7 +580,8 @@ def rows_decode(lb, rows, stream):
     del W, Y
     torch.cuda.empty_cache()
 
-    # (2) Qwen3-8B-shaped decode token, Q1_0 and Q2_0_g64, batch 1 (252 GEMVs, 36 layers)
+    # (2) Qwen3-8B-shaped decode token, Q1_0 and Q2_0_g64, batch 1 (252 GEMVs in 144 grouped
+    #     launches and 144 quantizations, 36 layers)
     for fmt in ("q2_0_g64", "q1_0"):
         make = make_q2_weights if fmt == "q2_0_g64" else make_q1_weights
         grouped = (lb.lb_gemv_q2_0_g64_grouped if fmt == "q2_0_g64"
@@ -605,8 +606,9 @@ def rows_decode(lb, rows, stream):
             for proj in layers:
                 for gi, members in enumerate(groups):
                     k = proj[members[0]][2]
-                    if gi in (0, 1, 3):  # new activation: attention input, attention out, FFN
-                        lb.lb_quantize_q8_0(xs[k], qs[k], ds[k], 1, k, stream=stream)
+                    # every group reads a new activation (attention input, attention output,
+                    # FFN input, FFN mid), quantized just before it
+                    lb.lb_quantize_q8_0(xs[k], qs[k], ds[k], 1, k, stream=stream)
                     mats = [(proj[i][0][0], proj[i][0][1], ybufs[i], None, proj[i][1])
                             for i in members]
                     grouped(mats, qs[k], ds[k], k, 1, stream=stream)
@@ -614,7 +616,7 @@ def rows_decode(lb, rows, stream):
         gbs = total / (ms * 1e-3) / 1e9
         rows[f"qwen3_8b_token_{fmt}_b1"] = {"GB/s": round(gbs, 1), "pct_hbm": round(100 * gbs / hbm, 1),
                                             "ms_per_token": round(ms, 4), "bytes": total,
-                                            "launches": 36 * 7}
+                                            "launches": 36 * 8}
         del layers
         torch.cuda.empty_cache()
 
@@ -644,9 +646,8 @@ def rows_decode(lb, rows, stream):
                 proj = body[7 * layer: 7 * layer + 7]
                 for gi, members in enumerate(groups):
                     k = proj[members[0]][2]
-                    if gi in (0, 1, 3):
-                        src = x2560 if k == 2560 else x
-                        lb.lb_quantize_i8_absmax(src, xq[k][0], xq[k][1], B, k, stream=stream)
+                    src = x2560 if k == 2560 else x  # a new activation for every group
+                    lb.lb_quantize_i8_absmax(src, xq[k][0], xq[k][1], B, k, stream=stream)
                     mats = [(proj[i][0], 0.02, ybs[i], None, proj[i][1]) for i in members]
                     lb.lb_gemv_trit_planes_grouped(mats, xq[k][0], xq[k][1], k, B,
                                                    stream=stream)
