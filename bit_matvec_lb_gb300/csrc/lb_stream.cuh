@@ -215,41 +215,6 @@ __device__ __forceinline__ int warp_sum_int(int v) {
     return v;
 }
 
-// Sums each of V per-lane values over the warp with VP - 1 + 5 - log2(VP) shuffles instead of
-// 5 V (VP = V rounded up to a power of two, at most 32).  At the step with lane distance o the
-// lanes with bit o set keep the upper half of the values still held, the others the lower half,
-// and each adds its partner's copy of the half it keeps; then the one value left is summed over
-// the remaining lane bits.  Lane l with l % (32 / VP) == 0 ends with the total of value
-// l / (32 / VP), which the return value carries (values >= V are zero).
-template <int V>
-struct PowTwo {
-    static constexpr int value = V <= 1 ? 1 : V <= 2 ? 2 : V <= 4 ? 4 : V <= 8 ? 8 : V <= 16 ? 16 : 32;
-    static constexpr int log2 = V <= 1 ? 0 : V <= 2 ? 1 : V <= 4 ? 2 : V <= 8 ? 3 : V <= 16 ? 4 : 5;
-};
-template <int V, typename T>
-__device__ __forceinline__ T warp_sum_many(const T (&in)[V], int lane) {
-    static_assert(V >= 1 && V <= 32, "at most 32 values");
-    constexpr int VP = PowTwo<V>::value;
-    T v[VP];
-#pragma unroll
-    for (int i = 0; i < VP; i++) v[i] = i < V ? in[i] : T(0);
-#pragma unroll
-    for (int k = 0; k < PowTwo<V>::log2; k++) {
-        const int o = 16 >> k, n = VP >> k;
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; i++) {
-            const T send = up ? v[i] : v[i + n / 2];
-            const T keep = up ? v[i + n / 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-#pragma unroll
-    for (int o = 16 >> PowTwo<V>::log2; o > 0; o >>= 1)
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-    return v[0];
-}
-
 // Matrix that owns row tile u, starting the search at `mi` (a CTA visits tiles in increasing
 // order, so the index only moves forward).
 __device__ __forceinline__ int find_mat(const StreamParams &p, int u, int mi) {
