@@ -879,15 +879,18 @@ constexpr int64_t kTcMinUnits = 64;
 template <int F>
 inline int dispatch_stream(StreamParams &p, int B, bool aux, int sms, cudaStream_t st) {
     p.fault = 0;
-    // Three or more tokens: the tensor-core variant (lb_tcgemv.cuh) when K is a multiple of
-    // its 256-column step, its activation operand (16 K bytes) fits in shared memory and the
-    // call has at least kTcMinUnits row units; the block-sum hook stays on the streaming
-    // kernels.
+    // Five or more tokens (four for Q2_0_g64): the tensor-core variant (lb_tcgemv.cuh) when K
+    // is a multiple of its 256-column step, its activation operand (16 K bytes) fits in shared
+    // memory and the call has at least kTcMinUnits row units; the block-sum hook stays on the
+    // streaming kernels.  Below that the lane-per-row kernel is faster (64 x 4096^2 at 3 tokens:
+    // Q2_0 2373 vs 2134 GB/s, Q1_0 1416 vs 1169, planar 2842 vs 1820; at 4 tokens Q1_0 1289 vs
+    // 1141, planar 2379 vs 1886, Q2_0 2075 vs 2118).
     int64_t tc_units = 0;
     for (int i = 0; i < p.G; i++) tc_units += (p.m[i].N + 127) / 128;
-    if (B >= 3 && !aux && p.K % 256 == 0 && p.K <= 4096 && tc_units >= kTcMinUnits) {
+    const int tc_min_tokens = F == kQ2 ? 4 : 5;
+    if (B >= tc_min_tokens && !aux && p.K % 256 == 0 && p.K <= 4096 &&
+        tc_units >= kTcMinUnits) {
         switch (B) {
-            case 3: return launch_tc_gemv<F, 3>(p, sms, st);
             case 4: return launch_tc_gemv<F, 4>(p, sms, st);
             case 5: return launch_tc_gemv<F, 5>(p, sms, st);
             case 6: return launch_tc_gemv<F, 6>(p, sms, st);

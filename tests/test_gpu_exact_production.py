@@ -8,7 +8,8 @@ no block-sum output, so they run the instantiations the bench times (no block-su
 
   * 1-2 tokens            -> the streaming kernel,
   * 3-8 tokens, K > 4096  -> the lane-per-row kernel,
-  * 3-8 tokens, K % 256 == 0, K <= 4096, >= 64 row units of 128 -> the tensor-core kernel.
+  * 4-8 tokens (Q2_0_g64) or 5-8 (Q1_0), K % 256 == 0, K <= 4096, >= 64 row units of 128
+    -> the tensor-core kernel (3 tokens, and 4 for Q1_0, -> the lane-per-row kernel).
 
 Planar outputs are bit-exact at every scale (their parity tests already compare bit patterns).
 """
@@ -88,7 +89,7 @@ def test_unit_scales_lane_per_row_kernel(qk, B, K):
 @pytest.mark.parametrize("B", [3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("K", [1024, 4096])
 def test_unit_scales_tensor_core_kernel(qk, B, K):
-    Ns = [130] * 31 + [77, 1]          # 65 row units of 128: the tensor-core kernel
+    Ns = [130] * 31 + [77, 1]          # 65 row units of 128: the tensor-core kernel from 4-5 tokens
     blocks = _unit_blocks(qk, sum(Ns), K, seed=7400 + K + B)
     q = synth.int8_codes(B, K, seed=7500 + B)
     want, dx = _expect(qk, blocks, q)

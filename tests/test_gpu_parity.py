@@ -442,12 +442,13 @@ def _q_group(qk, Ns, K, B, seed):
 
 
 @pytest.mark.parametrize("qk", [128, 64])
-@pytest.mark.parametrize("B", [3, 5, 8])
+@pytest.mark.parametrize("B", [3, 4, 5, 8])
 @pytest.mark.parametrize("K", [1024, 4096])
 def test_q_batched_tensor_core(qk, B, K):
-    """Batch 3..8 on the tensor-core kernel (grouped call with >= 64 row units, K a multiple of
-    256 up to the resident maximum 4096): every matrix, ragged ones and a single row included,
-    within the GEMV bound of the oracle."""
+    """A grouped call with >= 64 row units and K a multiple of 256 up to the resident maximum
+    4096 at 3..8 tokens: the tensor-core kernel from 4 tokens (Q2_0_g64) or 5 (Q1_0), the
+    lane-per-row kernel below; every matrix, ragged ones and a single row included, within the
+    GEMV bound of the oracle."""
     q, dx, outs = _q_group(qk, _tc_group_rows(), K, B, seed=640 + B + K)
     prod = oracle.q1_0_product if qk == 128 else oracle.q2_0_g64_product
     for blocks, y in outs:
@@ -456,10 +457,10 @@ def test_q_batched_tensor_core(qk, B, K):
         assert ok, worst
 
 
-@pytest.mark.parametrize("B", [3, 8])
+@pytest.mark.parametrize("B", [3, 4, 5, 8])
 def test_trit_batched_tensor_core(B):
-    """Planar at batch 3..8 on the tensor-core kernel: bit-exact accumulators and outputs for
-    every matrix of a grouped call with >= 64 row units."""
+    """Planar at batch 3..8 in a grouped call with >= 64 row units (the tensor-core kernel from 5
+    tokens, the lane-per-row kernel below): bit-exact accumulators and outputs for every matrix."""
     Ns, K = _tc_group_rows(), 2560
     planes, _ = synth.trit_planes(sum(Ns), K, seed=660 + B)
     x = synth.activations(B, K, seed=670 + B)
