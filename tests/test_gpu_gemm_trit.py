@@ -200,3 +200,34 @@ def test_quantize_tiles_then_gemm(M, K, Ns):
             assert np.array_equal(host(acc), acc_ref)
             assert np.array_equal(host(y).view(np.uint32), y_ref.view(np.uint32))
     assert lb.lb_device_status() == 0
+
+
+def test_quantize_tiles_degenerate_rows():
+    """The operand-writing quantizer on degenerate tokens: an all-zero row (x_scale 0, every code
+    0), a row whose extremes quantize to -127 and +127, a row of one nonzero value, and M = 1
+    past which the whole 128-row tile is zero; q, x_scale, acc and y bit-identical to the
+    oracle."""
+    for M, K in ((130, 128), (1, 256)):
+        x = synth.activations(M, K, seed=9300 + M)
+        x[0] = 0.0
+        if M > 2:
+            x[1] *= 1e30
+            x[2] = 0.0
+            x[2, K // 3] = -3.5
+        q_ref, xs_ref = oracle.quantize_i8_absmax(x)
+        q = guarded((M, K), torch.int8)
+        xs = guarded((M,), torch.float32, float("nan"))
+        ws = guarded(lb.lb_gemm_trit_workspace_bytes(M, K), torch.uint8, 0xFF)
+        lb.lb_quantize_i8_absmax_tiles(dev(x), q, xs, M, K, ws)
+        planes, _ = synth.trit_planes(200, K, seed=9310 + M)
+        y = guarded((M, 200), torch.float32, float("nan"))
+        acc = guarded((M, 200), torch.int32)
+        lb.lb_gemm_trit_planes_grouped_tiles([(dev(planes), 0.03, y, acc, 200)], xs, M, K, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(q), q_ref)
+        assert np.array_equal(host(xs).view(np.uint32),
+                              np.asarray(xs_ref, np.float32).view(np.uint32))
+        acc_ref, y_ref = oracle.trit_planes_product(planes, 0.03, q_ref, xs_ref)
+        assert np.array_equal(host(acc), acc_ref)
+        assert np.array_equal(host(y).view(np.uint32), y_ref.view(np.uint32))
+    assert lb.lb_device_status() == 0
