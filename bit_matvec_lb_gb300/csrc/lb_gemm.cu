@@ -899,6 +899,9 @@ __global__ void __launch_bounds__(kTritThreads, 1)
         const int npass = halves == 1 ? 1 : 2;
         const int ngrp = halves == 1 ? 2 : 1;    // 128-column groups per pass
         const int pitch = ngrp * kTileN + 4;      // partial row pitch in floats (conflict-free)
+        // Rows of y 16-byte aligned (y is, and N a multiple of 4) and no integer output: the
+        // partials are scaled as they are parked and every token row leaves in one bulk copy.
+        const bool bulk = W.acc == nullptr && (W.N & 3) == 0;
         for (int pass = 0; pass < npass; pass++) {
             const int64_t nbase = n0 + pass * kTileN;
             if (warp < kTritExpWarps) {
@@ -909,6 +912,7 @@ __global__ void __launch_bounds__(kTritThreads, 1)
                     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) +
                                         (uint32_t)(h * kTritTileN + pass * kTileN + g * kTileN);
                     const int row = h * kTileM + q * 32 + lane;
+                    const float xs = m0 + row < p.M ? p.x_scale[m0 + row] : 0.f;
 #pragma unroll 1
                     for (int c = 0; c < kTileN / 32; c++) {
                         uint32_t r[32];
@@ -916,6 +920,12 @@ __global__ void __launch_bounds__(kTritThreads, 1)
                         tmem_ld32(tl + 32 * c, r);
                         float4 *dst =
                             reinterpret_cast<float4 *>(part + row * pitch + g * kTileN + 32 * c);
+                        if (bulk) {
+#pragma unroll
+                            for (int v = 0; v < 32; v++)
+                                r[v] = __float_as_uint(__fmul_rn(
+                                    __fmul_rn(__uint_as_float(r[v]), xs), W.w_scale));
+                        }
 #pragma unroll
                         for (int v = 0; v < 8; v++)
                             dst[v] = make_float4(__uint_as_float(r[4 * v]),
@@ -923,10 +933,23 @@ __global__ void __launch_bounds__(kTritThreads, 1)
                                                  __uint_as_float(r[4 * v + 2]),
                                                  __uint_as_float(r[4 * v + 3]));
                     }
+                    if (bulk) fence_proxy_async_smem();  // parked rows -> the bulk copies
                 }
             }
             __syncthreads();
-            if (warp < kTritExpWarps && nbase < W.N) {
+            if (bulk) {
+                const int rr = threadIdx.x;  // one token row per thread of warps 0-7
+                if (rr < halves * kTileM && m0 + rr < p.M && nbase < W.N) {
+                    const int cols = (int)min((int64_t)ngrp * kTileN, (int64_t)W.N - nbase);
+                    bulk_s2g(W.y + (m0 + rr) * (int64_t)W.N + nbase, part + rr * pitch,
+                             (uint32_t)cols * 4u);
+                    bulk_commit();
+                    if (pass + 1 < npass)
+                        bulk_wait_read();
+                    else
+                        bulk_wait_all();
+                }
+            } else if (warp < kTritExpWarps && nbase < W.N) {
                 const int nrows = halves * kTileM;
                 for (int rr = warp; rr < nrows; rr += kTritExpWarps) {
                     if (m0 + rr >= p.M) break;  // rows run upward: the rest is past M as well

@@ -143,6 +143,34 @@ def test_gemm_trit_grouped():
         assert np.array_equal(host(y).view(np.uint32), y1.view(np.uint32))
 
 
+def test_gemm_trit_y_only_outputs():
+    """Grouped calls with no integer output, the form in which each token row of y leaves its CTA
+    as one bulk copy (N a multiple of 4), beside matrices whose rows take per-thread stores (N
+    not a multiple of 4; an integer output).  M = 300 over 44 weight tiles: two-token-tile CTAs
+    parking 128 columns per pass and a last pair holding one token tile; M = 100 with K too
+    short to split: one-token-tile CTAs parking 256 columns.  Column tails of 4 and 4 + 256;
+    every output bit-exact against the oracle, every guard band untouched."""
+    K = 128
+    for M, Ns in ((300, (9732, 4, 260, 130, 132)), (100, (260, 4, 130, 516, 132))):
+        q, xs = _acts(M, K, seed=M + 5)
+        ws = guarded(lb.lb_gemm_trit_workspace_bytes(M, K), torch.uint8)
+        mats, outs = [], []
+        for i, n in enumerate(Ns):
+            planes, _ = synth.trit_planes(n, K, seed=300 + 10 * M + i)
+            w = synth.w_scale(310 + i)
+            y = guarded((M, n), torch.float32, float("nan"))
+            acc = guarded((M, n), torch.int32, -7) if i == len(Ns) - 1 else None
+            mats.append((dev(planes), w, y, acc, n))
+            outs.append((planes, w, y, acc))
+        lb.lb_gemm_trit_planes_grouped(mats, dev(q), dev(xs), M, K, ws)
+        torch.cuda.synchronize()
+        for planes, w, y, acc in outs:
+            acc_ref, y_ref = oracle.trit_planes_product(planes, w, q, xs)
+            assert np.array_equal(host(y).view(np.uint32), y_ref.view(np.uint32)), planes.shape
+            if acc is not None:
+                assert np.array_equal(host(acc), acc_ref)
+
+
 @pytest.mark.parametrize("name,N,K", [("q", 2560, 2560), ("gate", 6912, 2560),
                                       ("down", 2560, 6912), ("k", 640, 2560)])
 def test_gemm_trit_prefill_shapes_sampled(name, N, K):
