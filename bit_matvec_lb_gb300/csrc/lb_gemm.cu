@@ -161,7 +161,7 @@ __device__ __forceinline__ bool wait_or_report(uint64_t *bar, uint32_t parity, i
     return false;
 }
 
-// Index and phase parity of a ring of N stages (N a power of two), advanced one step at a time.
+// Index and phase parity of a ring of N stages, advanced one step at a time.
 template <int N>
 struct Ring {
     int idx = 0;
