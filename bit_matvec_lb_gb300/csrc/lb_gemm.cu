@@ -895,7 +895,8 @@ __global__ void __launch_bounds__(kTritThreads, 1)
         // One CTA per tile: the partials are parked in the idle stage ring as [token][column]
         // tiles -- all 256 weight rows at once for one token tile (128 x 256 fits), in two passes
         // of 128 rows for two -- by warps 0-7 (lane quarter w % 4; token tile, or with one token
-        // tile column half, w / 4), then written row by row.
+        // tile column half, w / 4), then written to y row by row: one bulk copy per token row,
+        // or per-thread stores (a warp writes 128 columns per instruction).
         const int npass = halves == 1 ? 1 : 2;
         const int ngrp = halves == 1 ? 2 : 1;    // 128-column groups per pass
         const int pitch = ngrp * kTileN + 4;      // partial row pitch in floats (conflict-free)
