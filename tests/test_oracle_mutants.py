@@ -53,6 +53,11 @@ MUTANTS = [
     ("base3_high_digit_first", "int j = (int)((col % 80) / 5), i = (int)(col % 5);",
      "int j = (int)((col % 80) / 5), i = 4 - (int)(col % 5);"),
     ("base3_group_of_64", "int64_t g = col / 80;", "int64_t g = col / 64;"),
+    ("i8_amax_signed", "float a = fabsf(xb[k]);", "float a = xb[k];"),
+    ("i8_amax_first_token", "float a = fabsf(xb[k]);", "float a = fabsf(x[k]);"),
+    ("i8_round_half_away", "float v = round_half_even(xb[k] * s);", "float v = roundf(xb[k] * s);"),
+    ("i8_multiplier_from_scale", "float s = (amax != 0.0f) ? 127.0f / amax : 0.0f;",
+     "float s = (amax != 0.0f) ? 1.0f / (amax / 127.0f) : 0.0f;"),
     ("q_mag_signed", "m += fabs(term);", "m += term;"),
     ("q_mag_without_isum", "m += fabs(term);", "m += fabs((double)dw * (double)dxf) * 32.0 * 128.0;"),
 ]

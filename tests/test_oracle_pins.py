@@ -132,12 +132,24 @@ def test_q8_0_scaled_grid():
 
 
 def test_i8_absmax_quantizer():
-    x = np.array([[-2.0, 1.0, 0.5, 0.0, 2.0, -1.0, 0.25, 0.75]], dtype=np.float32)
+    x = np.array([[-2.0, 1.0, 0.5, 0.0, 2.0, -1.0, 0.25, 0.75],
+                  [-127.0, 2.5, 0.5, -3.5, 1.5, 126.5, -0.5, 3.0],
+                  [1.375, -0.6875, 0.6875, 0.0, 0.0, 0.0, 0.0, -1.375]], dtype=np.float32)
     q, s = oracle.quantize_i8_absmax(x)
-    # multiplier 127/2 = 63.5 exactly: 1 -> 63.5 -> 64 (tie to even), 0.5 -> 31.75 -> 32,
-    # 0.25 -> 15.875 -> 16, 0.75 -> 47.625 -> 48, -1 -> -63.5 -> -64
+    # token 0: multiplier 127/2 = 63.5 exactly: 1 -> 63.5 -> 64 (tie to even), 0.5 -> 31.75 ->
+    # 32, 0.25 -> 15.875 -> 16, 0.75 -> 47.625 -> 48, -1 -> -63.5 -> -64
     assert q[0].tolist() == [-127, 64, 32, 0, 127, -64, 16, 48]
     assert s[0] == np.float32(2.0) / np.float32(127.0)
+    # token 1 has its own absmax (127, taken by a negative value: the multiplier is exactly 1),
+    # and its ties go to the even neighbour: 2.5 -> 2, 0.5 -> 0, -3.5 -> -4, 1.5 -> 2,
+    # 126.5 -> 126, -0.5 -> 0
+    assert q[1].tolist() == [-127, 2, 0, -4, 2, 126, 0, 3]
+    assert s[1] == np.float32(1.0)
+    # token 2: the multiplier is 127 / 1.375 = 92.3636... rounded once, to 92.363640 in binary32
+    # (1 / (1.375 / 127) would give 92.363632); 0.6875 times it is 63.500004, just above the
+    # tie, so +-0.6875 -> +-64 (the other multiplier gives 63.499996 -> +-63)
+    assert q[2].tolist() == [127, -64, 64, 0, 0, 0, 0, -127]
+    assert s[2] == np.float32(1.375) / np.float32(127.0)
     q0, s0 = oracle.quantize_i8_absmax(np.zeros((1, 16), np.float32))
     assert not q0.any() and s0[0] == 0.0
 
