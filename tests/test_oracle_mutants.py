@@ -58,6 +58,11 @@ MUTANTS = [
     ("i8_round_half_away", "float v = round_half_even(xb[k] * s);", "float v = roundf(xb[k] * s);"),
     ("i8_multiplier_from_scale", "float s = (amax != 0.0f) ? 127.0f / amax : 0.0f;",
      "float s = (amax != 0.0f) ? 1.0f / (amax / 127.0f) : 0.0f;"),
+    ("bf16_transposed_weight", "oracle_bf16_to_f32(w[n * K + k])", "oracle_bf16_to_f32(w[k * N + n])"),
+    ("bf16_mag_signed", "m += fabs(p);", "m += p;"),
+    ("repack_padding_one", "scales[n * S + blk] = 0;", "scales[n * S + blk] = 0x3c00;"),
+    ("dequant_first_block_scale", "float d = oracle_f16_to_f32(block_scale_bits(block18));",
+     "float d = oracle_f16_to_f32(block_scale_bits(blocks + n * nblk * 18));"),
     ("q_mag_signed", "m += fabs(term);", "m += term;"),
     ("q_mag_without_isum", "m += fabs(term);", "m += fabs((double)dw * (double)dxf) * 32.0 * 128.0;"),
 ]
