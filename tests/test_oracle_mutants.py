@@ -63,6 +63,10 @@ MUTANTS = [
     ("repack_padding_one", "scales[n * S + blk] = 0;", "scales[n * S + blk] = 0x3c00;"),
     ("dequant_first_block_scale", "float d = oracle_f16_to_f32(block_scale_bits(block18));",
      "float d = oracle_f16_to_f32(block_scale_bits(blocks + n * nblk * 18));"),
+    ("planar_first_token_only", "int64_t x = q[b * K + g * 64 + c];", "int64_t x = q[g * 64 + c];"),
+    ("planar_beats_column_major",
+     "uint64_t pos = planes[(r * nbeat + g) * 2 + 0];\n                uint64_t neg = planes[(r * nbeat + g) * 2 + 1];",
+     "uint64_t pos = planes[(g * N + r) * 2 + 0];\n                uint64_t neg = planes[(g * N + r) * 2 + 1];"),
     ("q_mag_signed", "m += fabs(term);", "m += term;"),
     ("q_mag_without_isum", "m += fabs(term);", "m += fabs((double)dw * (double)dxf) * 32.0 * 128.0;"),
 ]
