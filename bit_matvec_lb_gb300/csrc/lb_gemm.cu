@@ -560,10 +560,11 @@ int gemm_q_with_workspace(int q2, const uint8_t *bits, const uint16_t *scales, c
 // partial tiles in its own shared memory, and after a cluster barrier the CTAs add the partials
 // of their share of the rows over the whole cluster (distributed shared memory).
 //   Tile: 256 tokens (two 128-token tensor-memory accumulators) x 256 weight rows, one
-//   M = 128, N = 256 MMA per token tile and 16-deep step.  Shared-memory bandwidth bounds this
-//   kernel (the tensor core reads both operands from it, and the copies and the weight expansion
-//   write it): N = 256 MMAs read a quarter fewer operand bytes per product than N = 128 ones, and
-//   one activation tile feeds 256 weight rows, one expanded weight tile 256 tokens.
+//   M = 128, N = 256 MMA per token tile and 16-deep step.  Shared memory feeds the tensor core
+//   both operands and takes the copies and the weight expansion: N = 256 MMAs read a quarter
+//   fewer operand bytes per product than N = 128 ones, and one activation tile feeds 256 weight
+//   rows, one expanded weight tile 256 tokens.  Measured: with two token tiles per CTA the main
+//   loop runs at the MMA rate; with one (small calls) a stage takes about twice its MMA time.
 //   Warp roles in a 320-thread CTA (one per SM): warps 0-7 expand weights (thread = weight row)
 //   and then read the accumulators out, warp 8 copies activation tiles (one 8 KB bulk copy per
 //   lane: one thread's copies are served one after another), warp 9 owns tensor memory and
