@@ -63,6 +63,15 @@ def q1_bytes(N, K):
     return N * (K // 128) * 18
 
 
+def trit_bytes(N, K):
+    """Planar ternary weights: one 16-byte {pos, neg} beat per 64 columns of a row."""
+    return N * (K // 64) * 16
+
+
+def bf16_bytes(N, K):
+    return N * K * 2
+
+
 def peaks(tensor: bool = False):
     """HBM GB/s (or, with tensor=True, dense bf16 TFLOP/s burst) and whether it was measured."""
     key, fallback = ("bf16_tflops", 1900.0) if tensor else ("hbm_gbs", 6800.0)
@@ -528,7 +537,7 @@ def rows_stream(lb, rows, stream):
             act = K + K // 16
         else:
             W1 = [synth.device_trit_planes(N, K, 52_000 + r) for r in range(N_ROT)]
-            wbytes = N * K // 64 * 16
+            wbytes = trit_bytes(N, K)
             grp = [(W1[r], 0.02, Y1[r], None, N) for r in range(N_ROT)]
 
             def quant():
@@ -627,9 +636,9 @@ def rows_decode(lb, rows, stream):
         for p, (name, n, k) in enumerate(synth.BITNET_2B4T_PROJ):
             planes = synth.device_trit_planes(n, k, synth.proj_seed(70_000, layer, p))
             body.append((planes, n, k))
-            body_bytes += n * k // 64 * 16
+            body_bytes += trit_bytes(n, k)
     HN, HK = synth.BITNET_HEAD
-    head = synth.device_bytes(HN * HK * 2, 80_000).view(torch.int16)
+    head = synth.device_bytes(bf16_bytes(HN, HK), 80_000).view(torch.int16)
     head = (head & 0x3FFF) | 0x3C00  # finite bf16 patterns
     for B in (1, 8):
         x = torch.from_numpy(synth.activations(B, 6912, seed=2)).cuda()
@@ -658,11 +667,11 @@ def rows_decode(lb, rows, stream):
 
         ms = time_graph(Graph(token_bitnet, stream), reps=20)
         ms_head = time_graph(Graph(head_only, stream), reps=20)
-        tot = body_bytes + HN * HK * 2
+        tot = body_bytes + bf16_bytes(HN, HK)
         rows[f"bitnet_2b4t_token_b{B}"] = {
             "GB/s": round(tot / (ms * 1e-3) / 1e9, 1), "pct_hbm": round(100 * tot / (ms * 1e-3) / 1e9 / hbm, 1),
             "ms_per_token": round(ms, 4), "bytes": tot,
-            "head_GB/s": round(HN * HK * 2 / (ms_head * 1e-3) / 1e9, 1),
+            "head_GB/s": round(bf16_bytes(HN, HK) / (ms_head * 1e-3) / 1e9, 1),
             "body_GB/s": round(body_bytes / ((ms - ms_head) * 1e-3) / 1e9, 1)}
 
 
@@ -690,7 +699,7 @@ def rows_dequant(lb, rows, stream):
             for t, out in zip(Wt, outs):
                 lb.lb_dequantize_trit_planes(t, 0.02, N, K, fmt, out, stream=stream)
         for label, fn, wbytes in (("q2_0_g64", q2pass, q2_bytes(N, K) + N * scale_stride(K, 64) * 2 - N * (K // 64) * 2),
-                                  ("trit_planes", tpass, N * K // 64 * 16)):
+                                  ("trit_planes", tpass, trit_bytes(N, K))):
             ms = time_graph(Graph(fn, stream), reps=20) / R
             gbs = (wbytes + N * K * esz) / (ms * 1e-3) / 1e9
             rows[f"dequant_{label}_4096x4096_{name}"] = {
